@@ -316,6 +316,22 @@ def pin_tolerance_rule():
     slack = 2e-3 * a + 1e-5
     assert orc.within_tolerance(y_ref + 0.99 * slack, y_ref, a).all()
     assert not orc.within_tolerance(y_ref + 1.01 * slack, y_ref, a).any()
+    # stored outputs: the nearest bfloat16 / binary16 of the exact value always passes, even with
+    # a == |y| where 2e-3 * a is below the format's own rounding error
+    rng = np.random.default_rng(11)
+    y = rng.standard_normal(20000) * np.exp2(rng.integers(-20, 20, 20000))
+    bf = torch.from_numpy(y).to(torch.bfloat16).to(torch.float64).numpy()
+    f16 = y.astype(np.float16).astype(np.float64)
+    zero = np.zeros_like(y)
+    assert orc.within_tolerance(bf, y, zero, "bf16").all()
+    assert orc.within_tolerance(f16[np.abs(y) < 6e4], y[np.abs(y) < 6e4], zero[np.abs(y) < 6e4], "f16").all()
+    # half an ulp exactly: 4.39 sits in the bfloat16 binade [4, 8) with ulp 2^-5
+    assert np.isclose(orc.output_half_ulp(4.39, "bf16"), 2.0 ** -6)
+    assert np.isclose(orc.output_half_ulp(4.39, "f16"), 2.0 ** -9)
+    assert np.isclose(orc.output_half_ulp(1e-9, "f16"), 2.0 ** -25)
+    # one full ulp off is rejected when a == 0
+    assert not orc.within_tolerance(np.array([4.0 + 2.0 ** -5 + 2.0 ** -9]), np.array([4.0]), np.array([0.0]),
+                                    "bf16").any()
 
 
 ALL_PINS = [pin_f16_decode_exhaustive, pin_bf16_decode_exhaustive, pin_f16_encode, pin_sizes,
