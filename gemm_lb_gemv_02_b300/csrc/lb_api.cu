@@ -1,0 +1,203 @@
+// liblb C ABI: argument validation, error reporting and dispatch to the kernel launchers.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "lb_common.cuh"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+std::mutex g_pack_mutex;
+
+// Sticky device error bits (one instance per device context; see lb_device_error).
+__device__ uint32_t g_device_error;
+
+constexpr int kMaxDevices = 64;
+uint32_t* g_error_ptr[kMaxDevices] = {};
+std::mutex g_error_ptr_mutex;
+
+}  // namespace
+
+namespace lb {
+
+lb_status fail(lb_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+lb_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(LB_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  return n;
+}
+
+uint32_t* device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_error_ptr_mutex);
+  if (!g_error_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    g_error_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  return g_error_ptr[dev];
+}
+
+}  // namespace lb
+
+using lb::fail;
+
+namespace {
+
+lb_status check_shape(int64_t n, int64_t k) {
+  if (n < 1) return fail(LB_ERR_SHAPE, "n must be >= 1 (got %lld)", (long long)n);
+  if (k < lb::kGroup || k % lb::kGroup)
+    return fail(LB_ERR_SHAPE, "k must be a positive multiple of 128 (got %lld)", (long long)k);
+  if (n > (int64_t(1) << 31) || k > (int64_t(1) << 24))
+    return fail(LB_ERR_SHAPE, "n = %lld or k = %lld beyond the supported range", (long long)n, (long long)k);
+  return LB_OK;
+}
+
+lb_status check_weight(const lb_weight* W) {
+  if (!W) return fail(LB_ERR_NULL, "W is NULL");
+  if (W->fmt != LB_FMT_1BIT_G128 && W->fmt != LB_FMT_TERNARY_G128)
+    return fail(LB_ERR_DTYPE, "unknown weight format %d", (int)W->fmt);
+  lb_status s = check_shape(W->n, W->k);
+  if (s != LB_OK) return s;
+  if (!W->codes || !W->scales) return fail(LB_ERR_NULL, "W->codes or W->scales is NULL");
+  if (!lb::aligned16(W->codes) || !lb::aligned16(W->scales))
+    return fail(LB_ERR_ALIGN, "W->codes and W->scales must be 16-byte aligned");
+  return LB_OK;
+}
+
+bool valid_dtype(int d) { return d == LB_F16 || d == LB_BF16; }
+
+}  // namespace
+
+extern "C" {
+
+const char* lb_status_string(lb_status s) {
+  switch (s) {
+    case LB_OK: return "LB_OK";
+    case LB_ERR_NULL: return "LB_ERR_NULL: a required pointer is NULL";
+    case LB_ERR_SHAPE: return "LB_ERR_SHAPE: invalid matrix shape or batch";
+    case LB_ERR_ALIGN: return "LB_ERR_ALIGN: a device pointer is not 16-byte aligned";
+    case LB_ERR_DTYPE: return "LB_ERR_DTYPE: unknown data type or weight format";
+    case LB_ERR_CODE: return "LB_ERR_CODE: ternary code outside {-1, 0, +1}";
+    case LB_ERR_NONFINITE: return "LB_ERR_NONFINITE: NaN or Inf among the weights";
+    case LB_ERR_RANGE: return "LB_ERR_RANGE: value outside the binary16 range";
+    case LB_ERR_CUDA: return "LB_ERR_CUDA: CUDA call failed";
+    case LB_ERR_UNSUPPORTED: return "LB_ERR_UNSUPPORTED: not implemented";
+    case LB_ERR_WORKSPACE: return "LB_ERR_WORKSPACE: workspace missing or too small";
+  }
+  return "unknown lb_status";
+}
+
+const char* lb_last_error(void) { return g_last_error; }
+
+int lb_version(void) { return 100; }
+
+lb_status lb_packed_bytes(int fmt, int64_t n, int64_t k, size_t* codes_bytes, size_t* scales_bytes) {
+  if (!codes_bytes || !scales_bytes) return fail(LB_ERR_NULL, "output pointer is NULL");
+  if (fmt != LB_FMT_1BIT_G128 && fmt != LB_FMT_TERNARY_G128) return fail(LB_ERR_DTYPE, "unknown format %d", fmt);
+  lb_status s = check_shape(n, k);
+  if (s != LB_OK) return s;
+  *codes_bytes = static_cast<size_t>(n) * static_cast<size_t>(k) / (fmt == LB_FMT_1BIT_G128 ? 8 : 4);
+  *scales_bytes = static_cast<size_t>(n) * static_cast<size_t>(k / lb::kGroup) * 2;
+  return LB_OK;
+}
+
+lb_status lb_pack_1bit(const float* w, int64_t n, int64_t k, uint8_t* codes, uint16_t* scales,
+                       lb_stream stream) {
+  lb_status s = check_shape(n, k);
+  if (s != LB_OK) return s;
+  if (!w || !codes || !scales) return fail(LB_ERR_NULL, "w, codes and scales must be non-NULL");
+  if (!lb::aligned16(w) || !lb::aligned16(codes) || !lb::aligned16(scales))
+    return fail(LB_ERR_ALIGN, "w, codes and scales must be 16-byte aligned");
+  std::lock_guard<std::mutex> lk(g_pack_mutex);
+  uint32_t flags = 0;
+  s = lb::launch_pack_1bit(w, n, k, codes, scales, reinterpret_cast<cudaStream_t>(stream), &flags);
+  if (s != LB_OK) return s;
+  if (flags & lb::kPackNonFinite) return fail(LB_ERR_NONFINITE, "weights contain NaN or Inf");
+  if (flags & lb::kPackRange) return fail(LB_ERR_RANGE, "a group max |w| rounds to binary16 infinity");
+  return LB_OK;
+}
+
+lb_status lb_pack_ternary(const int8_t* t, const uint16_t* s_in, int64_t n, int64_t k, uint8_t* codes,
+                          uint16_t* scales, lb_stream stream) {
+  lb_status s = check_shape(n, k);
+  if (s != LB_OK) return s;
+  if (!t || !s_in || !codes || !scales) return fail(LB_ERR_NULL, "t, s_in, codes and scales must be non-NULL");
+  if (!lb::aligned16(t) || !lb::aligned16(s_in) || !lb::aligned16(codes) || !lb::aligned16(scales))
+    return fail(LB_ERR_ALIGN, "t, s_in, codes and scales must be 16-byte aligned");
+  std::lock_guard<std::mutex> lk(g_pack_mutex);
+  uint32_t flags = 0;
+  s = lb::launch_pack_ternary(t, s_in, n, k, codes, scales, reinterpret_cast<cudaStream_t>(stream), &flags);
+  if (s != LB_OK) return s;
+  if (flags & lb::kPackCode) return fail(LB_ERR_CODE, "a ternary code is outside {-1, 0, +1}");
+  return LB_OK;
+}
+
+lb_status lb_gemv(const lb_weight* W, const void* x, int xdt, int batch, void* y, lb_stream stream) {
+  lb_status s = check_weight(W);
+  if (s != LB_OK) return s;
+  if (!x || !y) return fail(LB_ERR_NULL, "x and y must be non-NULL");
+  if (!valid_dtype(xdt)) return fail(LB_ERR_DTYPE, "unknown activation dtype %d", xdt);
+  if (batch < 1 || batch > 8) return fail(LB_ERR_SHAPE, "batch must be in [1, 8] (got %d)", batch);
+  if (!lb::aligned16(x) || !lb::aligned16(y)) return fail(LB_ERR_ALIGN, "x and y must be 16-byte aligned");
+  return lb::launch_gemv(*W, x, xdt, batch, y, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lb_status lb_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, int xdt, size_t* bytes) {
+  if (!bytes) return fail(LB_ERR_NULL, "bytes is NULL");
+  if (!valid_dtype(xdt)) return fail(LB_ERR_DTYPE, "unknown activation dtype %d", xdt);
+  if (m < 1) return fail(LB_ERR_SHAPE, "m must be >= 1");
+  lb_status s = check_shape(n, k);
+  if (s != LB_OK) return s;
+  *bytes = lb::gemm_workspace_bytes(m, k);
+  return LB_OK;
+}
+
+lb_status lb_gemm(const lb_weight* W, const void* x, int xdt, int64_t m, void* y, int ydt, void* workspace,
+                  size_t workspace_bytes, lb_stream stream) {
+  lb_status s = check_weight(W);
+  if (s != LB_OK) return s;
+  if (!x || !y) return fail(LB_ERR_NULL, "x and y must be non-NULL");
+  if (!valid_dtype(xdt) || !valid_dtype(ydt)) return fail(LB_ERR_DTYPE, "unknown dtype (x %d, y %d)", xdt, ydt);
+  if (m < 1 || m > (int64_t(1) << 24)) return fail(LB_ERR_SHAPE, "m must be in [1, 2^24] (got %lld)", (long long)m);
+  if (W->n % 16) return fail(LB_ERR_SHAPE, "lb_gemm needs n %% 16 == 0 (got %lld)", (long long)W->n);
+  if (W->fmt != LB_FMT_TERNARY_G128) return fail(LB_ERR_UNSUPPORTED, "lb_gemm implements the ternary format only");
+  if (!lb::aligned16(x) || !lb::aligned16(y)) return fail(LB_ERR_ALIGN, "x and y must be 16-byte aligned");
+  const size_t need = lb::gemm_workspace_bytes(m, W->k);
+  if (need && (!workspace || workspace_bytes < need))
+    return fail(LB_ERR_WORKSPACE, "workspace of %zu bytes needed (got %zu)", need, workspace_bytes);
+  if (need && (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(LB_ERR_ALIGN, "workspace must be 256-byte aligned");
+  return lb::launch_gemm(*W, x, xdt, m, y, ydt, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lb_status lb_device_error(uint32_t* word, int clear) {
+  if (!word) return fail(LB_ERR_NULL, "word is NULL");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return lb::cuda_fail(e, "lb_device_error: cudaDeviceSynchronize");
+  e = cudaMemcpyFromSymbol(word, g_device_error, sizeof(uint32_t));
+  if (e != cudaSuccess) return lb::cuda_fail(e, "lb_device_error: read");
+  if (clear) {
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(uint32_t));
+    if (e != cudaSuccess) return lb::cuda_fail(e, "lb_device_error: clear");
+  }
+  return LB_OK;
+}
+
+}  // extern "C"

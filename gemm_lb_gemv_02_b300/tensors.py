@@ -1,0 +1,84 @@
+"""Convenience wrappers over the C ABI that allocate outputs as torch CUDA tensors.
+
+Every function calls exactly one liblb entry point (plus torch allocations); no arithmetic of the
+method happens here.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import lb
+
+_TORCH = {lb.LB_F16: torch.float16, lb.LB_BF16: torch.bfloat16}
+
+
+def dtype_code(t: torch.dtype) -> int:
+    if t == torch.float16:
+        return lb.LB_F16
+    if t == torch.bfloat16:
+        return lb.LB_BF16
+    raise TypeError(f"activations must be float16 or bfloat16, got {t}")
+
+
+@dataclass
+class PackedWeight:
+    """A packed matrix on the device: codes uint8 plane + scales (binary16 bits, int16 storage)."""
+    fmt: int
+    n: int
+    k: int
+    codes: torch.Tensor
+    scales: torch.Tensor
+
+    def struct(self) -> lb.lb_weight:
+        return lb.make_weight(self.fmt, self.n, self.k, self.codes, self.scales)
+
+    @classmethod
+    def empty(cls, fmt: int, n: int, k: int, device="cuda") -> "PackedWeight":
+        cb, sb = lb.lb_packed_bytes(fmt, n, k)
+        return cls(fmt, n, k, torch.empty(cb, dtype=torch.uint8, device=device),
+                   torch.empty(sb // 2, dtype=torch.int16, device=device))
+
+
+def pack_1bit(w: torch.Tensor, stream=None) -> PackedWeight:
+    """fp32 [n][k] CUDA tensor -> PackedWeight via lb_pack_1bit."""
+    assert w.is_cuda and w.dtype == torch.float32 and w.is_contiguous() and w.dim() == 2
+    n, k = w.shape
+    pw = PackedWeight.empty(lb.LB_FMT_1BIT_G128, n, k, device=w.device)
+    lb.lb_pack_1bit(w, n, k, pw.codes, pw.scales, stream)
+    return pw
+
+
+def pack_ternary(t: torch.Tensor, s: torch.Tensor, stream=None) -> PackedWeight:
+    """int8 codes [n][k] + binary16 scales [n][k/128] (int16 or float16 storage) -> PackedWeight."""
+    assert t.is_cuda and t.dtype == torch.int8 and t.is_contiguous() and t.dim() == 2
+    n, k = t.shape
+    pw = PackedWeight.empty(lb.LB_FMT_TERNARY_G128, n, k, device=t.device)
+    lb.lb_pack_ternary(t, s.contiguous(), n, k, pw.codes, pw.scales, stream)
+    return pw
+
+
+def gemv(W: PackedWeight, x: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y[b][n] = W x[b] for x [batch][k] (batch 1..8), output in the dtype of x."""
+    assert x.is_cuda and x.is_contiguous() and x.dim() == 2 and x.shape[1] == W.k
+    if y is None:
+        y = torch.empty(x.shape[0], W.n, dtype=x.dtype, device=x.device)
+    lb.lb_gemv(W.struct(), x, dtype_code(x.dtype), x.shape[0], y, stream)
+    return y
+
+
+def gemm(W: PackedWeight, x: torch.Tensor, out_dtype: torch.dtype = torch.bfloat16,
+         y: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Y[m][n] = X W^T for X [m][k]; output dtype out_dtype."""
+    assert x.is_cuda and x.is_contiguous() and x.dim() == 2 and x.shape[1] == W.k
+    m = x.shape[0]
+    xdt = dtype_code(x.dtype)
+    if y is None:
+        y = torch.empty(m, W.n, dtype=out_dtype, device=x.device)
+    need = lb.lb_gemm_workspace_bytes(m, W.n, W.k, xdt)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    lb.lb_gemm(W.struct(), x, xdt, m, y, dtype_code(y.dtype), workspace, workspace.numel(), stream)
+    return y

@@ -1,0 +1,174 @@
+/*
+ * lb.h — C ABI of liblb: products against Bonsai-style low-bit weights on B300 (sm_103a).
+ *
+ * Weight formats (group size 128 along K; one IEEE binary16 scale per group; w = s_g * t_i):
+ *   - 1-bit ("Q1_0_g128"): t in {-1,+1}; bit 0 -> -scale, bit 1 -> +scale; 16 B of bits + 2 B of
+ *     scale per 128 weights = 1.125 bits per weight.  Defined by 7minutos.es, "Un tutorial de
+ *     codificacion para ejecutar PrismML Bonsai 1-bit LLM en CUDA con GGUF", section
+ *     "7 · Q1_0_g128 Cuantización" (representation box and Python demo).
+ *   - ternary: t in {-1,0,+1} with the same FP16 group scale (7minutos.es, "PrismML lanza
+ *     Bonsai 27B: compilaciones ternarias y de 1 bit", section "Cómo funciona la compresión"),
+ *     stored as 2-bit fields f = t + 1 (0 -> -1, 1 -> 0, 2 -> +1; 3 is invalid): 32 B of codes
+ *     + 2 B of scale per 128 weights = 2.125 bits per weight.
+ *
+ * Packed layout of an N x K matrix (rows n = output features, K = reduction, K % 128 == 0),
+ * two planes, both row-major and contiguous:
+ *   codes : 1-bit   uint8 [N][K/8],  weight k of row n = bit (k % 8) of byte k/8 (LSB first)
+ *           ternary uint8 [N][K/4],  weight k of row n = bits 2(k%4)..2(k%4)+1 of byte k/4
+ *   scales: uint16  [N][K/128], the binary16 bit pattern of the scale of group k/128 of row n
+ *
+ * Activations and outputs are row-major [rows][K] / [rows][N] arrays of binary16 (LB_F16) or
+ * bfloat16 (LB_BF16) values; all accumulation is FP32.
+ *
+ * Conventions shared by every entry point:
+ *   - All data pointers are DEVICE pointers owned by the caller (allocated with cudaMalloc or a
+ *     framework allocator); the library never frees them and keeps no reference after a call.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream); work is enqueued on it.
+ *   - Errors are returned as lb_status and never abort the process; nothing traps on the GPU.
+ *     lb_last_error() returns a thread-local text for the last failing call of this thread.
+ *   - lb_gemv / lb_gemm validate their arguments on the host and then launch asynchronously:
+ *     LB_OK means "enqueued".  The pack calls synchronise `stream` to read the device-side
+ *     validation result, so their LB_OK means "done and valid".
+ *   - Thread safety: every call may be made from any host thread; pack calls serialise on an
+ *     internal mutex (they share one device-side validation word per device).
+ */
+#ifndef LB_H_
+#define LB_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same underlying type as cudaStream_t; declared here so that this header needs no CUDA headers. */
+typedef struct CUstream_st* lb_stream;
+
+typedef enum lb_status {
+  LB_OK = 0,
+  LB_ERR_NULL = 1,        /* a required pointer is NULL                                        */
+  LB_ERR_SHAPE = 2,       /* n < 1, k < 128 or k % 128 != 0, batch outside [1, 8], m < 1       */
+  LB_ERR_ALIGN = 3,       /* a device pointer is not 16-byte aligned                          */
+  LB_ERR_DTYPE = 4,       /* unknown lb_dtype / lb_format                                      */
+  LB_ERR_CODE = 5,        /* a ternary code outside {-1, 0, +1} (pack_ternary)                 */
+  LB_ERR_NONFINITE = 6,   /* NaN or Inf among the fp32 weights (pack_1bit)                      */
+  LB_ERR_RANGE = 7,       /* a group max |w| rounds to binary16 infinity (pack_1bit)            */
+  LB_ERR_CUDA = 8,        /* a CUDA runtime/driver call failed; see lb_last_error()           */
+  LB_ERR_UNSUPPORTED = 9, /* valid request this build does not implement                      */
+  LB_ERR_WORKSPACE = 10   /* workspace pointer/size smaller than lb_gemm_workspace_bytes()    */
+} lb_status;
+
+typedef enum lb_format { LB_FMT_1BIT_G128 = 1, LB_FMT_TERNARY_G128 = 2 } lb_format;
+
+typedef enum lb_dtype { LB_F16 = 1, LB_BF16 = 2 } lb_dtype;
+
+/* A packed weight matrix; all pointers are device pointers owned by the caller. */
+typedef struct lb_weight {
+  int32_t fmt;            /* lb_format                                                         */
+  int32_t reserved;       /* must be 0                                                         */
+  int64_t n;              /* rows (output features), >= 1                                      */
+  int64_t k;              /* columns (reduction length), a positive multiple of 128            */
+  const uint8_t* codes;   /* codes plane, 16-byte aligned                                      */
+  const uint16_t* scales; /* scales plane, 16-byte aligned                                     */
+} lb_weight;
+
+/* Text for a status code (static storage). */
+const char* lb_status_string(lb_status s);
+
+/* Thread-local description of the last failing call on this thread ("" if none). */
+const char* lb_last_error(void);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int lb_version(void);
+
+/*
+ * Byte sizes of the two planes of an n x k matrix in format `fmt` (pure host arithmetic):
+ *   1-bit:   codes = n*k/8, scales = n*(k/128)*2   (18 bytes per group, 7minutos.es tutorial, §7 demo)
+ *   ternary: codes = n*k/4, scales = n*(k/128)*2   (34 bytes per group)
+ * Errors: LB_ERR_NULL (an output pointer is NULL), LB_ERR_SHAPE, LB_ERR_DTYPE (unknown fmt).
+ */
+lb_status lb_packed_bytes(int fmt, int64_t n, int64_t k, size_t* codes_bytes, size_t* scales_bytes);
+
+/*
+ * 1-bit sign / max-abs quantiser (7minutos.es tutorial, section "7 · Q1_0_g128 Cuantización",
+ * Python demo): for every row n and group g of 128 weights,
+ *     scale[n][g] = binary16_RNE( max_i |w[n][128g+i]| )      (maximum taken exactly in fp32)
+ *     bit i       = 1 if w[n][128g+i] >= 0 else 0              (+0.0 and -0.0 give 1)
+ *
+ * w      : device float32 [n][k], row-major, 16-byte aligned, read only.
+ * codes  : device uint8 [n][k/8] (output), 16-byte aligned.
+ * scales : device uint16 [n][k/128] (output), 16-byte aligned.
+ * Synchronous: the call synchronises `stream` and then reports
+ *   LB_ERR_NONFINITE if any weight is NaN/Inf, LB_ERR_RANGE if a group maximum rounds to
+ *   binary16 infinity (|w| >= 65520).  On these errors the outputs are unspecified.
+ */
+lb_status lb_pack_1bit(const float* w, int64_t n, int64_t k, uint8_t* codes, uint16_t* scales,
+                       lb_stream stream);
+
+/*
+ * Ternary packer (7minutos.es, "PrismML lanza Bonsai 27B", section "Cómo funciona la compresión";
+ * kerneldigest.dev, "Bonsai 2 27B", section "Arquitectura del Sistema"): codes are given, not
+ * quantised.  Writes field t + 1 for every weight and copies the scales bit for bit.
+ *
+ * t      : device int8 [n][k], values in {-1, 0, +1}, 16-byte aligned.
+ * s_in   : device uint16 [n][k/128] binary16 scale patterns, 16-byte aligned.
+ * codes  : device uint8 [n][k/4] (output); scales: device uint16 [n][k/128] (output; may equal s_in).
+ * Synchronous; returns LB_ERR_CODE if any t is outside {-1, 0, +1} (outputs then unspecified).
+ */
+lb_status lb_pack_ternary(const int8_t* t, const uint16_t* s_in, int64_t n, int64_t k,
+                          uint8_t* codes, uint16_t* scales, lb_stream stream);
+
+/*
+ * Decode GEMV and small-batch GEMV (7minutos.es, "PrismML lanza Bonsai 27B", section
+ * "Rendimiento y decodificación especulativa DSpark": generation is memory-bandwidth bound;
+ * speculative verification of k = 4 drafted tokens runs the target at width k + 1):
+ *     y[b][n] = sum_g s[n][g] * sum_{i<128} t[n][128g+i] * x[b][128g+i],   0 <= b < batch,
+ * with FP32 accumulation, rounded once to the dtype of x (round to nearest even).
+ *
+ * W     : packed matrix (n x k).
+ * x     : device [batch][k] of `xdt`, 16-byte aligned.     y : device [batch][n] of `xdt`.
+ * batch : 1 .. 8.
+ * Asynchronous on `stream`.  Errors (no launch): LB_ERR_NULL, LB_ERR_SHAPE, LB_ERR_ALIGN,
+ * LB_ERR_DTYPE; LB_ERR_CUDA if the launch fails.
+ */
+lb_status lb_gemv(const lb_weight* W, const void* x, int xdt, int batch, void* y, lb_stream stream);
+
+/*
+ * Workspace bytes that lb_gemm needs for an m x k activation matrix of dtype `xdt` against an
+ * n x k weight (0 means none is needed).  Pure host arithmetic.
+ */
+lb_status lb_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, int xdt, size_t* bytes);
+
+/*
+ * Prefill GEMM (same product as lb_gemv for m token rows; 7minutos.es, "PrismML lanza Bonsai
+ * 27B", section "Rendimiento …": prefill is compute bound):
+ *     Y[r][n] = sum_g s[n][g] * sum_{i<128} t[n][128g+i] * X[r][128g+i],   0 <= r < m,
+ * FP32 accumulation on the tensor cores, output rounded to `ydt` (RNE).
+ *
+ * W                : packed matrix (n x k); n must be a multiple of 16.
+ * x                : device [m][k] of `xdt`, 16-byte aligned.  Values must lie in the binary16
+ *                    range |x| <= 65504 (the product runs on FP16 tensor-core operands, where
+ *                    s * t is exact); bfloat16 inputs are converted to binary16 first.
+ * y                : device [m][n] of `ydt`, 16-byte aligned.
+ * workspace        : device scratch of at least lb_gemm_workspace_bytes(...) bytes, 256-byte
+ *                    aligned, used only during this call's kernels (may be reused afterwards).
+ * Asynchronous on `stream`.  Errors (no launch): LB_ERR_NULL, LB_ERR_SHAPE, LB_ERR_ALIGN,
+ * LB_ERR_DTYPE, LB_ERR_WORKSPACE; LB_ERR_UNSUPPORTED for the 1-bit format; LB_ERR_CUDA.
+ */
+lb_status lb_gemm(const lb_weight* W, const void* x, int xdt, int64_t m, void* y, int ydt,
+                  void* workspace, size_t workspace_bytes, lb_stream stream);
+
+/*
+ * Sticky device-side error word of the current device (0 = none).  Kernels that wait on an
+ * mbarrier give up after a bounded number of polls, set a bit here and return instead of
+ * hanging.  lb_device_error() synchronises the device, reads the word and, if `clear` is
+ * non-zero, resets it.  Bit 0: a GEMM pipeline wait timed out.
+ */
+lb_status lb_device_error(uint32_t* word, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LB_H_ */

@@ -1,0 +1,97 @@
+"""The C ABI library loads and exports every symbol include/lb.h declares; host-side argument
+validation returns the documented status before touching the GPU (runs without a GPU)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from gemm_lb_gemv_02_b300 import lb
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "lb.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(lb_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_expected_entry_points():
+    names = declared_functions()
+    assert set(names) == set(lb.EXPORTED), names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(lb.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings():
+    for code, name in lb.STATUS_NAMES.items():
+        assert lb.lb_status_string(code).startswith(name)
+
+
+def test_packed_bytes():
+    assert lb.lb_packed_bytes(lb.LB_FMT_1BIT_G128, 2048, 2048) == (2048 * 2048 // 8, 2048 * 16 * 2)
+    assert lb.lb_packed_bytes(lb.LB_FMT_TERNARY_G128, 17408, 5120) == (17408 * 5120 // 4, 17408 * 40 * 2)
+    for bad in ((lb.LB_FMT_1BIT_G128, 0, 128), (lb.LB_FMT_1BIT_G128, 4, 100), (lb.LB_FMT_1BIT_G128, 4, 0)):
+        with pytest.raises(lb.LBError) as e:
+            lb.lb_packed_bytes(*bad)
+        assert e.value.name == "LB_ERR_SHAPE"
+    with pytest.raises(lb.LBError) as e:
+        lb.lb_packed_bytes(7, 4, 128)
+    assert e.value.name == "LB_ERR_DTYPE"
+
+
+def _status(fn, *args):
+    try:
+        fn(*args)
+    except lb.LBError as e:
+        return e.name
+    return "LB_OK"
+
+
+# Fake, never-dereferenced device addresses: validation must reject before any CUDA call.
+A16 = 0x10000
+MIS = 0x10001
+
+
+def test_pack_validation():
+    assert _status(lb.lb_pack_1bit, None, 4, 128, A16, A16, 0) == "LB_ERR_NULL"
+    assert _status(lb.lb_pack_1bit, A16, 4, 100, A16, A16, 0) == "LB_ERR_SHAPE"
+    assert _status(lb.lb_pack_1bit, A16, 0, 128, A16, A16, 0) == "LB_ERR_SHAPE"
+    assert _status(lb.lb_pack_1bit, MIS, 4, 128, A16, A16, 0) == "LB_ERR_ALIGN"
+    assert _status(lb.lb_pack_ternary, A16, None, 4, 128, A16, A16, 0) == "LB_ERR_NULL"
+    assert _status(lb.lb_pack_ternary, A16, A16, 4, 129, A16, A16, 0) == "LB_ERR_SHAPE"
+    assert _status(lb.lb_pack_ternary, A16, A16, 4, 128, MIS, A16, 0) == "LB_ERR_ALIGN"
+
+
+def test_gemv_validation():
+    W = lb.make_weight(lb.LB_FMT_1BIT_G128, 16, 128, A16, A16)
+    assert _status(lb.lb_gemv, W, None, lb.LB_F16, 1, A16, 0) == "LB_ERR_NULL"
+    assert _status(lb.lb_gemv, W, A16, 9, 1, A16, 0) == "LB_ERR_DTYPE"
+    assert _status(lb.lb_gemv, W, A16, lb.LB_F16, 0, A16, 0) == "LB_ERR_SHAPE"
+    assert _status(lb.lb_gemv, W, A16, lb.LB_F16, 9, A16, 0) == "LB_ERR_SHAPE"
+    assert _status(lb.lb_gemv, W, MIS, lb.LB_F16, 1, A16, 0) == "LB_ERR_ALIGN"
+    assert _status(lb.lb_gemv, lb.make_weight(3, 16, 128, A16, A16), A16, lb.LB_F16, 1, A16, 0) == "LB_ERR_DTYPE"
+    assert _status(lb.lb_gemv, lb.make_weight(1, 16, 130, A16, A16), A16, lb.LB_F16, 1, A16, 0) == "LB_ERR_SHAPE"
+    assert _status(lb.lb_gemv, lb.make_weight(1, 16, 128, MIS, A16), A16, lb.LB_F16, 1, A16, 0) == "LB_ERR_ALIGN"
+    assert _status(lb.lb_gemv, lb.make_weight(1, 16, 128, None, A16), A16, lb.LB_F16, 1, A16, 0) == "LB_ERR_NULL"
+
+
+def test_gemm_validation():
+    W = lb.make_weight(lb.LB_FMT_TERNARY_G128, 256, 256, A16, A16)
+    need = lb.lb_gemm_workspace_bytes(5, 256, 256, lb.LB_BF16)
+    assert need == 128 * 256 * 2
+    assert _status(lb.lb_gemm, W, A16, lb.LB_BF16, 5, A16, lb.LB_BF16, None, 0, 0) == "LB_ERR_WORKSPACE"
+    assert _status(lb.lb_gemm, W, A16, lb.LB_BF16, 5, A16, lb.LB_BF16, A16, need - 1, 0) == "LB_ERR_WORKSPACE"
+    assert _status(lb.lb_gemm, W, A16, lb.LB_BF16, 5, A16, lb.LB_BF16, A16 + 16, need, 0) == "LB_ERR_ALIGN"
+    assert _status(lb.lb_gemm, W, A16, lb.LB_BF16, 0, A16, lb.LB_BF16, A16, need, 0) == "LB_ERR_SHAPE"
+    assert _status(lb.lb_gemm, lb.make_weight(2, 250, 256, A16, A16), A16, lb.LB_BF16, 5, A16, lb.LB_BF16,
+                   A16, need, 0) == "LB_ERR_SHAPE"
+    assert _status(lb.lb_gemm, lb.make_weight(1, 256, 256, A16, A16), A16, lb.LB_BF16, 5, A16, lb.LB_BF16,
+                   A16, need, 0) == "LB_ERR_UNSUPPORTED"
+    assert _status(lb.lb_gemm, W, A16, 5, 5, A16, lb.LB_BF16, A16, need, 0) == "LB_ERR_DTYPE"

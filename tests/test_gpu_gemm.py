@@ -1,0 +1,73 @@
+"""Prefill GEMM (tcgen05) on the GPU against the FP64 oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+from gemm_lb_gemv_02_b300 import synth
+from oracle import lb_oracle as orc
+from tests.helpers import check_products, oracle_pack, u16, u8
+
+pytestmark = pytest.mark.gpu
+
+lb = pytest.importorskip("gemm_lb_gemv_02_b300.lb")
+from gemm_lb_gemv_02_b300 import tensors  # noqa: E402
+
+
+def _ternary(n, k, seed):
+    inp = {"t": synth.ternary_codes(n, k, seed), "s": synth.ternary_scales_bits(n, k, 0.02, seed + 1)}
+    pw = tensors.pack_ternary(inp["t"].cuda(), inp["s"].cuda())
+    codes, scales = oracle_pack("ternary", inp)
+    return pw, codes, scales
+
+
+def _check(pw, codes, scales, x, out_dtype, what, rows=None, cols=None):
+    y = tensors.gemm(pw, x.cuda(), out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert lb.lb_device_error(clear=True) == 0
+    xs = x if rows is None else x[rows]
+    c, s = (codes, scales) if cols is None else (codes[cols], scales[cols])
+    xv = orc.decode_activation_bits(u16(xs), "bf16" if x.dtype == torch.bfloat16 else "f16")
+    y_ref, a = orc.gemm(orc.FMT_TERNARY, c, s, pw.k, xv)
+    yd = y if rows is None else y[torch.as_tensor(rows, device=y.device)]
+    return check_products(yd, y_ref, a, what, cols=cols)
+
+
+@pytest.mark.parametrize("m,n,k", [(1, 256, 128), (5, 16, 256), (128, 256, 384), (130, 272, 256),
+                                   (300, 512, 640), (64, 48, 1024)])
+@pytest.mark.parametrize("xdt", ["bf16", "f16"])
+def test_gemm_small_shapes(m, n, k, xdt):
+    pw, codes, scales = _ternary(n, k, seed=m + n + k)
+    x = synth.activations(m, k, xdt, seed=m * 3 + k)
+    for out in (torch.bfloat16, torch.float16):
+        _check(pw, codes, scales, x, out, f"gemm m={m} n={n} k={k} x={xdt} y={out}")
+
+
+def test_gemm_integer_exact():
+    m, n, k = 200, 256, 512
+    t = synth.ternary_codes(n, k, seed=21)
+    s = torch.full((n, k // 128), 0x3C00, dtype=torch.int16)
+    pw = tensors.pack_ternary(t.cuda(), s.cuda())
+    codes, scales = orc.pack_ternary(t.numpy(), s.numpy().view(np.uint16))
+    g = torch.Generator().manual_seed(22)
+    x = torch.randint(-3, 4, (m, k), generator=g).to(torch.bfloat16)
+    y = tensors.gemm(pw, x.cuda(), out_dtype=torch.float16)
+    torch.cuda.synchronize()
+    y_ref, _ = orc.gemm(orc.FMT_TERNARY, codes, scales, k, orc.bf16_bits_to_f64(u16(x)))
+    assert np.array_equal(orc.f16_bits_to_f64(u16(y)), y_ref)
+
+
+def test_gemm_c5_prefill_sampled():
+    """The 512 x 5120 -> 17408 prefill workload at full size, outputs checked on sampled rows and
+    columns (the whole GEMM runs; the oracle recomputes 96 token rows x 1200 weight rows)."""
+    wl = synth.WORKLOADS["c5"]
+    mat = wl.matrices[0]
+    inp = synth.matrix_inputs(wl, 0)
+    pw = tensors.pack_ternary(inp["t"].cuda(), inp["s"].cuda())
+    x = synth.workload_activations(wl, 0, 512)
+    codes = u8(pw.codes).reshape(mat.n, -1)
+    scales = u16(pw.scales).reshape(mat.n, -1)
+    rng = np.random.default_rng(5)
+    rows = np.unique(np.concatenate([[0, 127, 128, 511], rng.integers(0, 512, 92)]))
+    cols = np.unique(np.concatenate([np.arange(8), np.arange(mat.n - 8, mat.n), rng.integers(0, mat.n, 1184)]))
+    _check(pw, codes, scales, x, torch.bfloat16, "c5 prefill", rows=rows, cols=cols)

@@ -1,0 +1,123 @@
+"""Decode / small-batch GEMV on the GPU against the FP64 oracle (|y - y_ref| <= 2e-3 a + 1e-5)."""
+
+import numpy as np
+import pytest
+import torch
+
+from gemm_lb_gemv_02_b300 import synth
+from oracle import lb_oracle as orc
+from tests.helpers import check_products, oracle_pack, oracle_products, u16, u8
+
+pytestmark = pytest.mark.gpu
+
+lb = pytest.importorskip("gemm_lb_gemv_02_b300.lb")
+from gemm_lb_gemv_02_b300 import tensors  # noqa: E402
+
+TDT = {"f16": torch.float16, "bf16": torch.bfloat16}
+
+
+def _packed(fmt, n, k, seed):
+    if fmt == "1bit":
+        inp = {"w": synth.weights_fp32(n, k, 0.05, seed)}
+        pw = tensors.pack_1bit(inp["w"].cuda())
+    else:
+        inp = {"t": synth.ternary_codes(n, k, seed), "s": synth.ternary_scales_bits(n, k, 0.02, seed + 1)}
+        pw = tensors.pack_ternary(inp["t"].cuda(), inp["s"].cuda())
+    codes, scales = oracle_pack(fmt, inp)
+    return pw, codes, scales
+
+
+def _run_guarded(pw, x):
+    """gemv into the middle of a canary-filled buffer; checks the canaries afterwards."""
+    b, n = x.shape[0], pw.n
+    pad = 64
+    buf = torch.full((b * n + 2 * pad,), 12345, dtype=torch.int16, device="cuda")
+    y = buf[pad:pad + b * n].view(x.dtype).view(b, n)
+    tensors.gemv(pw, x, y)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:pad] == 12345) and torch.all(buf[pad + b * n:] == 12345), "write outside y"
+    return y
+
+
+@pytest.mark.parametrize("fmt", ["1bit", "ternary"])
+@pytest.mark.parametrize("xdt", ["f16", "bf16"])
+@pytest.mark.parametrize("n,k", [(1, 128), (7, 256), (16, 128), (17, 640), (100, 384), (333, 1024), (1100, 512)])
+def test_gemv_small_shapes(fmt, xdt, n, k):
+    pw, codes, scales = _packed(fmt, n, k, seed=n * 7 + k)
+    for batch in (1, 2, 3, 5, 8):
+        x = synth.activations(batch, k, xdt, seed=n + k + batch).cuda()
+        y = _run_guarded(pw, x)
+        y_ref, a = oracle_products(fmt, codes, scales, k, x.cpu())
+        check_products(y, y_ref, a, f"{fmt} {xdt} n={n} k={k} batch={batch}")
+
+
+@pytest.mark.parametrize("fmt", ["1bit", "ternary"])
+@pytest.mark.parametrize("xdt", ["f16", "bf16"])
+def test_gemv_integer_exact(fmt, xdt):
+    """Scales 1 and small-integer x: every partial sum is an exactly representable integer, so the
+    result must be exact (checks the decode offsets cancel exactly)."""
+    n, k = 64, 512
+    if fmt == "1bit":
+        w = synth.weights_fp32(n, k, 1.0, seed=11)
+        w[:, ::128] = 1.0                                          # group max |w| == 1 -> scale 1.0
+        w = w.clamp(-1.0, 1.0)
+        pw = tensors.pack_1bit(w.cuda())
+        codes, scales = orc.pack_1bit(w.numpy())
+    else:
+        t = synth.ternary_codes(n, k, seed=12)
+        s = torch.full((n, k // 128), 0x3C00, dtype=torch.int16)  # 1.0
+        pw = tensors.pack_ternary(t.cuda(), s.cuda())
+        codes, scales = orc.pack_ternary(t.numpy(), s.numpy().view(np.uint16))
+    assert np.all(scales == 0x3C00)
+    g = torch.Generator().manual_seed(13)
+    x = torch.randint(-4, 5, (4, k), generator=g).to(TDT[xdt])
+    y = tensors.gemv(pw, x.cuda())
+    torch.cuda.synchronize()
+    y_ref, _ = oracle_products(fmt, codes, scales, k, x)
+    yv = orc.decode_activation_bits(u16(y), xdt)
+    assert np.array_equal(yv, y_ref)
+
+
+def _workload_check(key, batch, sample_rows=None):
+    wl = synth.WORKLOADS[key]
+    worst = 0.0
+    for i, mat in enumerate(wl.matrices):
+        inp = synth.matrix_inputs(wl, i)
+        if wl.fmt == "1bit":
+            pw = tensors.pack_1bit(inp["w"].cuda())
+        else:
+            pw = tensors.pack_ternary(inp["t"].cuda(), inp["s"].cuda())
+        x = synth.workload_activations(wl, i, batch).cuda()
+        y = tensors.gemv(pw, x)
+        torch.cuda.synchronize()
+        rows = None
+        if sample_rows and mat.n > sample_rows:
+            rng = np.random.default_rng(i)
+            rows = np.unique(np.concatenate([np.arange(16), np.arange(mat.n - 16, mat.n),
+                                             rng.integers(0, mat.n, sample_rows)]))
+        # the oracle works from the device-packed planes (their bit-exactness is tested separately)
+        codes = u8(pw.codes).reshape(mat.n, -1)
+        scales = u16(pw.scales).reshape(mat.n, -1)
+        y_ref, a = oracle_products(wl.fmt, codes, scales, mat.k, x.cpu(), rows)
+        worst = max(worst, check_products(y, y_ref, a, f"{key}/{mat.name} batch={batch}", cols=rows))
+        del pw, x, y
+    return worst
+
+
+def test_gemv_c1_full():
+    _workload_check("c1", 1)
+
+
+def test_gemv_c2_layer_set_full():
+    _workload_check("c2", 1)
+
+
+@pytest.mark.parametrize("batch", [1, 4])
+def test_gemv_c3_lm_head(batch):
+    _workload_check("c3", batch, sample_rows=3000)
+
+
+@pytest.mark.parametrize("key", ["c4t", "c4b"])
+@pytest.mark.parametrize("batch", [1, 5])
+def test_gemv_c4_layer_set(key, batch):
+    _workload_check(key, batch, sample_rows=1500)
