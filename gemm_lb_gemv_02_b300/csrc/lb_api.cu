@@ -35,9 +35,12 @@ lb_status cuda_fail(cudaError_t e, const char* where) {
 }
 
 int sm_count() {
+  static int cached[kMaxDevices] = {};
   int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  if (cached[dev] > 0) return cached[dev];
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  cached[dev] = n;
   return n;
 }
 

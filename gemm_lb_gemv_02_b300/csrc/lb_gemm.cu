@@ -21,6 +21,8 @@
 //   * epilogue: warps 0-7 read the FP32 accumulator with tcgen05.ld and store BF16/FP16 rows.
 // Every mbarrier wait is bounded; a timeout sets a bit in the device error word and the CTA
 // finishes (TMEM is always released).
+#include <mutex>
+
 #include "lb_common.cuh"
 
 namespace {
@@ -290,9 +292,21 @@ lb_status launch_gemm(const lb_weight& W, const void* x, int xdt, int64_t m, voi
                                                                          static_cast<uint8_t*>(ws), err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "lb_gemm: prologue launch");
-  e = cudaFuncSetAttribute(gemm_ternary_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kSmemBytes));
-  if (e != cudaSuccess) return cuda_fail(e, "lb_gemm: set shared memory size");
+  {
+    // once per device: raise the dynamic shared-memory limit of the GEMM kernel
+    static std::mutex mu;
+    static bool done[64] = {};
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "lb_gemm: cudaGetDevice");
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev < 0 || dev >= 64 || !done[dev]) {
+      e = cudaFuncSetAttribute(gemm_ternary_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kSmemBytes));
+      if (e != cudaSuccess) return cuda_fail(e, "lb_gemm: set shared memory size");
+      if (dev >= 0 && dev < 64) done[dev] = true;
+    }
+  }
   const dim3 grid((n + BN - 1) / BN, static_cast<unsigned>(mpad / BM));
   gemm_ternary_kernel<<<grid, kThreads, kSmemBytes, st>>>(static_cast<const uint8_t*>(ws), W.codes, W.scales,
                                                           static_cast<uint16_t*>(y), static_cast<int>(m), n, k,

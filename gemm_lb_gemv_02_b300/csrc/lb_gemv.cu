@@ -6,263 +6,738 @@
 // and "Rendimiento y decodificación especulativa DSpark" for the bandwidth-bound decode and the
 // width-5 speculative verification.)
 //
-// Design.  A 1-bit GEMV must retire ~37 T weights/s to stream at 80% of B300 HBM bandwidth, about
-// one lane-operation per weight over the whole GPU; integer LOP3 issues at half rate on sm_103a,
-// so the per-weight multiply cannot stay on the CUDA cores.  The packed codes are therefore
-// decoded straight into FP16/BF16 tensor-core A fragments with one LOP3 per two weights and the
-// dot products run on mma.sync m16n8k16 (batch <= 8 fills its n = 8 columns):
+// Why tensor cores in a GEMV.  A 1-bit GEMV must retire ~37 T weights/s to stream at 80% of B300
+// HBM bandwidth, about one lane-operation per weight over the whole GPU, and integer LOP3 issues
+// at half rate on sm_103a.  The per-weight multiply-add therefore runs on mma.sync m16n8k16
+// (batch <= 8 fills its n = 8 columns), fed by a decode of one LOP3 per two weights:
 //
-//   * "offset exponent" decode: a half whose exponent encodes 2^(10-m) (fp16; 2^(7-m) for bf16)
-//     and whose mantissa bit m (ternary: bits m, m+1) is copied from the code word has the exact
-//     value o + b (o = 2^(10-m)), b the code bit (or 2-bit field).  One LOP3 builds two of them.
-//   * the tensor core returns D_g = sum (o_k + b_k) x_k for one 128-group; the per-column constant
-//     C_g = sum (o_k + c) x_k (c = 1/2 for 1-bit, 1 for ternary) comes from the same MMA with A
-//     set to the constants, so sum t x = 2 (D_g - C_g) for 1-bit (t = 2b - 1) and D_g - C_g for
-//     ternary (t = f - 1).  All A values are exact, products are exact in FP32, and the group scale
-//     is applied once per group in FP32: y += s * (D_g - C_g).
-//   * the MMA reduction order along K is free, so code bit j of a word lands in whichever k slot
-//     its register occupies and x is gathered into B fragments in the matching order.
+//   * "offset exponent" decode: a binary16 whose exponent encodes 2^(10-m) and whose mantissa bit
+//     m (ternary: bits m, m+1) is copied from the code word has the exact value o + b, o = 2^(10-m),
+//     b the code bit (2-bit field).  One LOP3 (mask held in a register, exponent as immediate)
+//     builds two such halves, i.e. one half2 A-fragment register.
+//   * per group g and batch column c the constant C_g[c] = sum_k (o_k + h) x[c][k] (h = 1/2 for
+//     1-bit, 1 for ternary) is computed once per CTA in FP32 and fed as the MMA's C operand -C_g,
+//     so the tensor core returns sum_k (b_k - h) x_k: sum t x / 2 for 1-bit (t = 2b - 1) and
+//     sum t x for ternary (t = f - 1).  A values and products are exact.
+//   * the group scale is applied once per group in FP32: acc += s * D_g; 1-bit doubles at the end.
+//   * the reduction order along K is free, so code bit j of a word lands in whichever k slot its
+//     register occupies; x is gathered once per CTA into B fragments in the matching order.
+//   * bfloat16 x is converted to binary16 after an exact power-of-two rescaling per batch column
+//     (undone on the FP32 result), so both activation types share the binary16 decode.
+//
+// Memory pipeline: a producer warp streams the codes (and scales) of 128-row x 8-group tiles with
+// 2-D TMA loads (128-byte swizzled, so the consumers' fragment reads hit 32 distinct banks) into a
+// ring of shared-memory stages.  Sixteen consumer warps work on the eight 16-row tiles of a row
+// block, two per tile, each taking half of a stage's groups; their partial sums meet in shared
+// memory at the end of the row block.  CTAs are persistent over row blocks.  When a matrix has
+// too few row blocks to fill the GPU, K is split across the CTAs of a thread-block cluster whose
+// partial sums meet in distributed shared memory.  The kernel is launched with programmatic
+// dependent launch: weight loads start before griddepcontrol.wait, which guards every read of x
+// and write of y.
+#include <cuda.h>
+
+#include <cstring>
+#include <mutex>
+
 #include "lb_common.cuh"
 
 namespace {
 
-// ----------------------------------------------------------------------------- decode constants
-// fp16 half with exponent for 2^(10-m), replicated in both halves; bf16: 2^(7-m).
-template <bool BF>
-__device__ __forceinline__ constexpr uint32_t expo(int m) {
-  return BF ? (static_cast<uint32_t>(134 - m) << 7) * 0x00010001u
-            : (static_cast<uint32_t>(25 - m) << 10) * 0x00010001u;
+constexpr int NT = 8;                     // 16-row tiles per row block
+constexpr int NW = 2 * NT;                // consumer warps: two per tile
+constexpr int ROWS = 16 * NT;             // rows per row block
+constexpr int kThreads = (NW + 1) * 32;   // + one TMA producer warp
+constexpr int kMaxCluster = 8;
+constexpr int GS = 8;                     // groups per pipeline stage
+constexpr int GH = GS / 2;                // groups per consumer warp per stage
+constexpr int kBox = 16384;               // one codes box: 128 rows x 128 bytes
+constexpr int kScaleBox = ROWS * 16;      // 128 rows x 8 binary16 scales
+constexpr int kSmemMax = 227 * 1024;
+
+template <int FMT>
+struct FmtTraits;
+template <>
+struct FmtTraits<1> {                     // 1-bit: 16 B per group per row, 8 groups per box
+  static constexpr int gbytes = 16, nb = 1, stages = 6;
+  static constexpr float h = 0.5f;
+};
+template <>
+struct FmtTraits<2> {                     // ternary: 32 B per group per row, 4 groups per box
+  static constexpr int gbytes = 32, nb = 2, stages = 3;
+  static constexpr float h = 1.0f;
+};
+
+// ----------------------------------------------------------------------------- decode
+__host__ __device__ constexpr uint32_t expo16(int m) {   // 2^(10-m) in both halves
+  return (static_cast<uint32_t>(25 - m) << 10) * 0x00010001u;
+}
+// 1-bit: register j of a 32-bit code word holds bits j (low half) and j+16 (high half) = weights
+// k = j and k = j + 16 of the word; mantissa position m_j in 1..9 (m >= 1 keeps o + 1/2 exact).
+__host__ __device__ constexpr int pos1(int j) { return j == 0 ? 1 : (j <= 9 ? j : j - 6); }
+// Ternary: register p of a 32-bit word (16 fields) holds field p (low) and p + 8 (high) = weights
+// k = p and k = p + 8 of the word; the field sits at mantissa bits (m, m+1), m in {0,2,4,6,8}.
+__host__ __device__ constexpr int pos2(int p) { return p <= 4 ? 2 * p : 2 * p - 6; }
+
+template <int FMT>
+__device__ __forceinline__ constexpr float reg_offset(int i) {
+  return static_cast<float>(1 << (10 - (FMT == 1 ? pos1(i) : pos2(i & 7))));
 }
 
-// 1-bit: register j (0..15) of a 32-bit code word holds bits j (low half) and j+16 (high half),
-// i.e. weights k = j and k = j + 16 of the word's 32.  Mantissa positions m >= 1 keep o + 1/2
-// exact (fp16: m in 1..9, bf16: m in 1..6).
-template <bool BF>
-__device__ __forceinline__ void decode_1bit(uint32_t w, uint32_t (&a)[16]) {
-  const uint32_t w1 = w << 1;
-  if (!BF) {
-    const uint32_t w6 = w >> 6;
-    a[0] = (w1 & (0x00010001u << 1)) | expo<false>(1);
-#pragma unroll
-    for (int j = 1; j <= 9; ++j) a[j] = (w & (0x00010001u << j)) | expo<false>(j);
-#pragma unroll
-    for (int j = 10; j <= 15; ++j) a[j] = (w6 & (0x00010001u << (j - 6))) | expo<false>(j - 6);
-  } else {
-    const uint32_t w6 = w >> 6, w12 = w >> 12;
-    a[0] = (w1 & (0x00010001u << 1)) | expo<true>(1);
-#pragma unroll
-    for (int j = 1; j <= 6; ++j) a[j] = (w & (0x00010001u << j)) | expo<true>(j);
-#pragma unroll
-    for (int j = 7; j <= 12; ++j) a[j] = (w6 & (0x00010001u << (j - 6))) | expo<true>(j - 6);
-#pragma unroll
-    for (int j = 13; j <= 15; ++j) a[j] = (w12 & (0x00010001u << (j - 12))) | expo<true>(j - 12);
+template <uint32_t E>
+__device__ __forceinline__ uint32_t lop_and_or(uint32_t src, uint32_t mask) {   // (src & mask) | E
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(src), "r"(mask), "n"(E));
+  return r;
+}
+
+// Decoder state for one 32-bit code word: the word and its shifted copies.
+struct Word1 {
+  uint32_t w, w1, w6;
+};
+__device__ __forceinline__ Word1 prep1(uint32_t w) { return Word1{w, w << 1, w >> 6}; }
+template <int J>
+__device__ __forceinline__ uint32_t dec1(const Word1& x, const uint32_t (&M)[10]) {
+  constexpr int m = pos1(J);
+  const uint32_t src = J == 0 ? x.w1 : (J <= 9 ? x.w : x.w6);
+  return lop_and_or<expo16(m)>(src, M[m]);
+}
+struct Word2 {
+  uint32_t w, w6;
+};
+__device__ __forceinline__ Word2 prep2(uint32_t w) { return Word2{w, w >> 6}; }
+template <int P>
+__device__ __forceinline__ uint32_t dec2(const Word2& x, const uint32_t (&M)[10]) {
+  constexpr int m = pos2(P);
+  return lop_and_or<expo16(m)>(P <= 4 ? x.w : x.w6, M[m]);
+}
+
+// A-fragment register I (0..15) of the lane's 32-k block of one row.
+template <int FMT, int I>
+__device__ __forceinline__ uint32_t areg(const Word1& a1, const Word2& a2lo, const Word2& a2hi,
+                                         const uint32_t (&M)[10]) {
+  if constexpr (FMT == 1) return dec1<I>(a1, M);
+  else return dec2<(I & 7)>(I < 8 ? a2lo : a2hi, M);
+}
+
+// D = A * B + C with C = {-C_g[2q], -C_g[2q+1], -C_g[2q], -C_g[2q+1]} (the baseline of my columns).
+__device__ __forceinline__ void mma_c4(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                       uint32_t b0, uint32_t b1, const float4& c) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%11,%12,%13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c.x), "f"(c.y), "f"(c.z), "f"(c.w));
+}
+__device__ __forceinline__ void mma_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ----------------------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_dsmem(uint32_t local_addr, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(NW * 32) : "memory"); }
+
+// Shared-memory loads with 32-bit shared addresses.  Loads from a pipeline slot are volatile, so
+// they stay between the barrier wait that makes the slot valid and the arrive that hands it back.
+// Loads from the CTA-private x / baseline region are plain asm whose addresses carry a token made
+// after the barrier that published the region, so they cannot be hoisted above it but otherwise
+// schedule freely.
+__device__ __forceinline__ uint32_t ldsv32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 ldsv64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float4 lds128f(uint32_t a) {
+  float4 v;
+  asm("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
+  return v;
+}
+
+struct alignas(64) Args {
+  CUtensorMap tm_codes;       // codes plane as a 2-D u8 tensor {code bytes per row, n}, box 128 x 128
+  CUtensorMap tm_scales;      // scales plane as a 2-D u16 tensor {G, n}, box 8 x 128 (if scales_tma)
+  const uint16_t* scales;
+  const uint16_t* x;
+  uint16_t* y;
+  uint32_t* err;
+  int n, k, batch, G;
+  int S;           // CTAs per cluster along K (chunk = cluster rank)
+  int gpc;         // groups per K chunk (a multiple of GS when S > 1)
+  int row_blocks;
+  int scales_tma;  // scales arrive in the stage through tm_scales
+};
+
+template <int FMT, int BP>
+struct Layout {
+  static constexpr int stages = FmtTraits<FMT>::stages;
+  static constexpr int slot = FmtTraits<FMT>::nb * kBox + kScaleBox;
+  static constexpr int ring = stages * slot;                     // 1024-byte aligned base
+  static constexpr int bars = ring;                              // full[stages], empty[stages]
+  static constexpr int red = bars + 128;                         // 2 x ROWS x 8 floats
+  static constexpr int colf = red + 2 * ROWS * 8 * 4;            // 8 column factors + 8 column maxima
+  static constexpr int cneg = colf + 64;                         // gpc x 4 x float4 {-C[2q], -C[2q+1], same}
+  static constexpr int xgroup = 4 * 4 * BP * 16;                 // x fragments of one group
+  __host__ __device__ static int xs(int gpc) { return cneg + gpc * 64; }
+  // + 512 bytes that lanes outside the batch may read past the last group, + 1024 alignment slack
+  __host__ __device__ static int total(int gpc) { return xs(gpc) + gpc * xgroup + 512 + 1024; }
+};
+
+template <int FMT, bool XBF, int BP>
+__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ Args a) {
+  using FT = FmtTraits<FMT>;
+  using L = Layout<FMT, BP>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024u - (lbdev::smem_u32(smem_raw) & 1023u)) & 1023u);   // 1024-aligned
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + L::bars);
+  uint64_t* empty = full + L::stages;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = a.S > 1 ? cluster_rank() : 0u;
+  const int gpc = a.gpc;
+  const int g_begin = static_cast<int>(rank) * gpc;
+  const int ng = min(gpc, a.G - g_begin);                        // groups of this CTA's chunk (>= 1)
+  const int nst = (ng + GS - 1) / GS;                            // stages per row block
+  const int rb_stride = gridDim.y;
+  const int my_rbs = (a.row_blocks - static_cast<int>(blockIdx.y) + rb_stride - 1) / rb_stride;
+  const int total_st = my_rbs * nst;
+  bool ok = true;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < L::stages; ++s) {
+      lbdev::mbar_init(&full[s], 1);
+      lbdev::mbar_init(&empty[s], NW);
+    }
+    lbdev::fence_mbar_init();
   }
-}
+  if (threadIdx.x < 8) reinterpret_cast<uint32_t*>(sm + L::colf)[8 + threadIdx.x] = 0u;   // column maxima
+  __syncthreads();
 
-template <bool BF>
-__device__ __forceinline__ int pos_1bit(int j) {
-  return BF ? (j == 0 ? 1 : j <= 6 ? j : j <= 12 ? j - 6 : j - 12) : (j == 0 ? 1 : j <= 9 ? j : j - 6);
-}
-
-// Constant A register for the 1-bit baseline: value o + 1/2 (mantissa bit m-1 set).
-template <bool BF>
-__device__ __forceinline__ uint32_t const_1bit(int j) {
-  const int m = pos_1bit<BF>(j);
-  return expo<BF>(m) | (0x00010001u << (m - 1));
-}
-
-// Ternary: register p (0..7) of a 32-bit code word (16 fields) holds field p (low half) and field
-// p + 8 (high half), i.e. weights k = p and k = p + 8 of the word's 16.  Field at mantissa bits
-// (m, m+1): fp16 m in {0,2,4,6,8}; bf16 m in {0,2,4}.
-template <bool BF>
-__device__ __forceinline__ int pos_tern(int p) {
-  return BF ? (p <= 2 ? 2 * p : p <= 5 ? 2 * p - 6 : 2 * p - 12) : (p <= 4 ? 2 * p : 2 * p - 6);
-}
-
-template <bool BF>
-__device__ __forceinline__ void decode_tern(uint32_t w, uint32_t* a) {
-  const uint32_t w6 = w >> 6;
-  if (!BF) {
+  if (warp == NW) {
+    // ======================= producer: weights do not depend on earlier kernels, so no wait
+    if (lane == 0) {
+      lbdev::prefetch_tmap(&a.tm_codes);
+      if (a.scales_tma) lbdev::prefetch_tmap(&a.tm_scales);
+      const uint32_t bytes = static_cast<uint32_t>(FT::nb * kBox + (a.scales_tma ? kScaleBox : 0));
+      for (int st = 0; st < total_st; ++st) {
+        const int s = st % L::stages;
+        if (!lbdev::mbar_wait(&empty[s], static_cast<uint32_t>(((st / L::stages) & 1) ^ 1))) { ok = false; break; }
+        const int row0 = (static_cast<int>(blockIdx.y) + (st / nst) * rb_stride) * ROWS;
+        const int g0 = g_begin + (st % nst) * GS;
+        uint8_t* slot = sm + s * L::slot;
+        lbdev::mbar_arrive_expect_tx(&full[s], bytes);
 #pragma unroll
-    for (int p = 0; p <= 4; ++p) a[p] = (w & (0x00030003u << (2 * p))) | expo<false>(2 * p);
-#pragma unroll
-    for (int p = 5; p <= 7; ++p) a[p] = (w6 & (0x00030003u << (2 * p - 6))) | expo<false>(2 * p - 6);
+        for (int b = 0; b < FT::nb; ++b)
+          lbdev::tma_load_2d(slot + b * kBox, &a.tm_codes, (g0 + b * (GS / FT::nb)) * FT::gbytes, row0, &full[s]);
+        if (a.scales_tma) lbdev::tma_load_2d(slot + FT::nb * kBox, &a.tm_scales, g0, row0, &full[s]);
+      }
+    }
+    __syncwarp();
+    griddep_launch();
   } else {
-    const uint32_t w12 = w >> 12;
+    // ======================= consumers
+    const int r = lane >> 2, q = lane & 3;
+    const int tile = warp & (NT - 1), half = warp / NT;
+    float* colf = reinterpret_cast<float*>(sm + L::colf);            // [8] factors, then [8] maxima
+    float* cneg = reinterpret_cast<float*>(sm + L::cneg);            // [gpc][4][4]
+    uint8_t* xs = sm + L::xs(gpc);
+    griddep_wait();                                   // x is read and y written only after this
+
+    // ---- x prologue.  Tuple (g, n, qq): the 32 activations x[n][128(g_begin+g) + 32qq ..] of one
+    // fragment lane.  bfloat16: first the per-column maximum over the chunk, then an exact 2^p.
+    const int tuples = ng * BP * 4;
+    auto load32 = [&](int t, uint32_t (&X)[16]) -> bool {
+      const int qq = t & 3, n = (t >> 2) % BP, g = (t >> 2) / BP;
+      if (t >= tuples || n >= a.batch) {
 #pragma unroll
-    for (int p = 0; p <= 2; ++p) a[p] = (w & (0x00030003u << (2 * p))) | expo<true>(2 * p);
-#pragma unroll
-    for (int p = 3; p <= 5; ++p) a[p] = (w6 & (0x00030003u << (2 * p - 6))) | expo<true>(2 * p - 6);
-#pragma unroll
-    for (int p = 6; p <= 7; ++p) a[p] = (w12 & (0x00030003u << (2 * p - 12))) | expo<true>(2 * p - 12);
-  }
-}
-
-// Constant A register for the ternary baseline: value o + 1 (mantissa bit m set).
-template <bool BF>
-__device__ __forceinline__ uint32_t const_tern(int p) {
-  const int m = pos_tern<BF>(p);
-  return expo<BF>(m) | (0x00010001u << m);
-}
-
-template <bool BF>
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  if (BF) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-  } else {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-  }
-}
-
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) { return __byte_perm(a, b, sel); }
-
-template <bool BF>
-__device__ __forceinline__ float to_f32(uint16_t h) {
-  return BF ? __uint_as_float(static_cast<uint32_t>(h) << 16) : __half2float(__ushort_as_half(h));
-}
-
-template <bool BF>
-__device__ __forceinline__ uint16_t from_f32(float v) {
-  return BF ? __bfloat16_as_ushort(__float2bfloat16_rn(v)) : __half_as_ushort(__float2half_rn(v));
-}
-
-// ----------------------------------------------------------------------------- the kernel
-// CTA = 4 warps over the same 16*T rows; warp w takes groups w, w+4, ...  Lane = (r, q) with
-// r = lane / 4 (rows r and r + 8 of each 16-row tile, and batch column r for the B fragment) and
-// q = lane % 4 (the quarter of the group this lane's code words cover).
-template <int FMT, bool BF, int T>
-__global__ void __launch_bounds__(128) gemv_mma_kernel(const uint8_t* __restrict__ codes,
-                                                       const uint16_t* __restrict__ scales,
-                                                       const uint16_t* __restrict__ x, uint16_t* __restrict__ y,
-                                                       int n_rows, int k, int batch) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int r = lane >> 2, q = lane & 3;
-  const int G = k / lb::kGroup;
-  const int row0 = blockIdx.x * (16 * T);
-  const int64_t crow = FMT == 1 ? k / 8 : k / 4;   // code bytes per row
-
-  float acc[T][4];
-#pragma unroll
-  for (int t = 0; t < T; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-
-  uint32_t cst[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) cst[j] = FMT == 1 ? const_1bit<BF>(j) : const_tern<BF>(j & 7);
-
-  for (int g = warp; g < G; g += 4) {
-    // ---- B fragments: x[r][128g + 32q + perm], gathered to match the decode order
-    uint32_t bx[16];
-    if (r < batch) {
-      const uint4* xp = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(r) * k + g * lb::kGroup + 32 * q);
-      uint32_t X[16];
+        for (int i = 0; i < 16; ++i) X[i] = 0u;
+        return false;
+      }
+      const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(n) * a.k +
+                                                        static_cast<int64_t>(g_begin + g) * 128 + 32 * qq);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const uint4 v = __ldg(xp + i);
+        const uint4 v = __ldg(src + i);
         X[4 * i] = v.x; X[4 * i + 1] = v.y; X[4 * i + 2] = v.z; X[4 * i + 3] = v.w;
       }
-      if (FMT == 1) {
+      return true;
+    };
+    if (XBF) {
+      uint32_t* cmax = reinterpret_cast<uint32_t*>(colf + 8);
+      for (int base = 0; base < tuples; base += NW * 32) {
+        const int t = base + static_cast<int>(threadIdx.x);
+        uint32_t X[16];
+        if (load32(t, X)) {
+          uint32_t mx = 0;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) bx[j] = prmt(X[j >> 1], X[(j >> 1) + 8], (j & 1) ? 0x7632 : 0x5410);
-      } else {
-#pragma unroll
-        for (int rr = 0; rr < 16; ++rr) {
-          const int uu = rr >> 3, p = rr & 7;
-          bx[rr] = prmt(X[8 * uu + (p >> 1)], X[8 * uu + (p >> 1) + 4], (p & 1) ? 0x7632 : 0x5410);
+          for (int i = 0; i < 16; ++i) mx = max(mx, max((X[i] << 16) & 0x7fffffffu, X[i] & 0x7fff0000u));
+          atomicMax(&cmax[(t >> 2) % BP], mx);          // IEEE bit patterns of |x| order like values
         }
       }
+      consumer_sync();
+    }
+    if (threadIdx.x < 8) {
+      float f = 1.f;
+      if (XBF) {
+        const uint32_t mx = reinterpret_cast<uint32_t*>(colf + 8)[threadIdx.x];
+        if (mx != 0u) {
+          const int e = static_cast<int>((mx >> 23) & 0xFF);
+          const int p = max(-126, min(126, 127 - e));                         // max * 2^p in [1, 2)
+          f = __uint_as_float(static_cast<uint32_t>(127 - p) << 23);          // 2^-p
+        }
+      }
+      colf[threadIdx.x] = f;
+    }
+    for (int base = 0; base < tuples; base += NW * 32) {          // uniform: quads stay together
+      const int t = base + static_cast<int>(threadIdx.x);
+      const int qq = t & 3, n = (t >> 2) % BP, g = (t >> 2) / BP;
+      uint32_t X[16];
+      const bool act = load32(t, X);
+      if (XBF && act) {
+        const uint32_t mx = reinterpret_cast<uint32_t*>(colf + 8)[n];
+        float scale = 1.f;
+        if (mx != 0u) {
+          const int e = static_cast<int>((mx >> 23) & 0xFF);
+          const int p = max(-126, min(126, 127 - e));
+          scale = __uint_as_float(static_cast<uint32_t>(127 + p) << 23);      // 2^p (exact)
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float lo = __uint_as_float(X[i] << 16) * scale, hi = __uint_as_float(X[i] & 0xffff0000u) * scale;
+          const __half2 h2 = __floats2half2_rn(lo, hi);
+          X[i] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+      }
+      uint32_t B[16];
+      float c = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        uint32_t lo_src, hi_src, sel;
+        if (FMT == 1) {
+          lo_src = X[i >> 1]; hi_src = X[(i >> 1) + 8]; sel = (i & 1) ? 0x7632 : 0x5410;
+        } else {
+          const int uu = i >> 3, p = i & 7;
+          lo_src = X[8 * uu + (p >> 1)]; hi_src = X[8 * uu + (p >> 1) + 4]; sel = (p & 1) ? 0x7632 : 0x5410;
+        }
+        B[i] = __byte_perm(lo_src, hi_src, sel);
+        const float2 fv = __half22float2(*reinterpret_cast<const __half2*>(&B[i]));
+        c = fmaf(reg_offset<FMT>(i) + FT::h, fv.x + fv.y, c);
+      }
+      c += __shfl_xor_sync(0xffffffffu, c, 1);
+      c += __shfl_xor_sync(0xffffffffu, c, 2);
+      if (t < tuples) {
+        uint8_t* dst = xs + g * L::xgroup + (n * 4 + qq) * 16;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<uint4*>(dst + i * (L::xgroup / 4)) = make_uint4(B[4 * i], B[4 * i + 1], B[4 * i + 2], B[4 * i + 3]);
+        if (qq == 0) {
+          const float v = act ? -c : 0.f;
+          cneg[g * 16 + (n >> 1) * 4 + (n & 1)] = v;
+          cneg[g * 16 + (n >> 1) * 4 + 2 + (n & 1)] = v;
+        }
+      }
+    }
+    for (int i = threadIdx.x; i < ng * 16; i += NW * 32) {          // columns beyond the padded batch
+      if (((i >> 2) & 3) * 2 + (i & 1) >= BP) cneg[i] = 0.f;
+    }
+    consumer_sync();
+
+    uint32_t tok;                                      // orders the private-region loads after the barrier
+    asm volatile("mov.u32 %0, 0;" : "=r"(tok)::"memory");
+
+    // ---- per-thread constants
+    uint32_t M[10];                                    // decode masks, kept in registers
+    constexpr uint32_t kMask = FMT == 1 ? 0x00010001u : 0x00030003u;
+#define LB_MASK(m) asm volatile("mov.b32 %0, %1;" : "=r"(M[m]) : "n"(kMask << (m)))
+    LB_MASK(0); LB_MASK(1); LB_MASK(2); LB_MASK(3); LB_MASK(4);
+    LB_MASK(5); LB_MASK(6); LB_MASK(7); LB_MASK(8); LB_MASK(9);
+#undef LB_MASK
+    const int ia = tile * 16 + r;                                  // rows ia and ia + 8 of the block
+    uint32_t pcode;                                                // this lane's words, first group of my half
+    if (FMT == 1) {
+      pcode = static_cast<uint32_t>(ia * 128) | (4u * q) | (static_cast<uint32_t>(r) << 4);
+      pcode ^= static_cast<uint32_t>(half * GH) << 4;
     } else {
-#pragma unroll
-      for (int j = 0; j < 16; ++j) bx[j] = 0u;
+      pcode = static_cast<uint32_t>(ia * 128) | (8u * (q & 1)) | (static_cast<uint32_t>((q >> 1) ^ r) << 4);
+      pcode += static_cast<uint32_t>(half * kBox);                 // ternary: one box per half
     }
-    // ---- per-column baseline C_g (identical for every row)
-    float cc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) mma16816<BF>(cc, cst[2 * i], cst[2 * i], cst[2 * i + 1], cst[2 * i + 1], bx[2 * i], bx[2 * i + 1]);
+    const uint32_t sm32 = lbdev::smem_u32(sm);
+    const uint32_t xs_lane = sm32 + static_cast<uint32_t>(L::xs(gpc)) + lane * 16 + tok;
+    const uint32_t cn_q = sm32 + static_cast<uint32_t>(L::cneg) + 16 * q + tok;
+    const uint32_t sc_off = static_cast<uint32_t>(FT::nb * kBox + ia * 16 + half * 8);
+    const float mul = FMT == 1 ? 2.f : 1.f;
+    const int c0col = 2 * q, c1col = 2 * q + 1;
+    const float f0 = colf[c0col] * mul, f1 = colf[c1col] * mul;   // output factors of my columns
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    int s = 0, cstage = 0, i_rb = 0;
+    uint32_t ph = 0;
 
+    for (int st = 0; st < total_st; ++st) {
+      const int rb = static_cast<int>(blockIdx.y) + i_rb * rb_stride;
+      const int g0 = cstage * GS + half * GH;                     // my first group, relative to g_begin
+      const int cnt = min(GH, ng - g0);                           // my groups in this stage (may be <= 0)
+      const uint32_t slot = sm32 + static_cast<uint32_t>(s * L::slot);
+      float sa[GH], sb[GH];
+      if (!a.scales_tma) {                                        // fallback: scales from L2
+        const int row_a = rb * ROWS + ia, row_b = row_a + 8;
 #pragma unroll
-    for (int t = 0; t < T; ++t) {
-      const int ra = row0 + 16 * t + r, rb = ra + 8;
-      uint32_t A[16], B8[16];
-      float sa = 0.f, sb = 0.f;
-      if (FMT == 1) {
-        uint32_t wa = 0, wb = 0;
-        if (ra < n_rows) {
-          wa = __ldg(reinterpret_cast<const uint32_t*>(codes + ra * crow + 16 * g) + q);
-          sa = __half2float(__ushort_as_half(__ldg(scales + static_cast<int64_t>(ra) * G + g)));
+        for (int j = 0; j < GH; ++j) {
+          sa[j] = 0.f; sb[j] = 0.f;
+          if (j < cnt) {
+            const int64_t g = g_begin + g0 + j;
+            if (row_a < a.n) sa[j] = __half2float(__ushort_as_half(__ldg(a.scales + static_cast<int64_t>(row_a) * a.G + g)));
+            if (row_b < a.n) sb[j] = __half2float(__ushort_as_half(__ldg(a.scales + static_cast<int64_t>(row_b) * a.G + g)));
+          }
         }
-        if (rb < n_rows) {
-          wb = __ldg(reinterpret_cast<const uint32_t*>(codes + rb * crow + 16 * g) + q);
-          sb = __half2float(__ushort_as_half(__ldg(scales + static_cast<int64_t>(rb) * G + g)));
-        }
-        decode_1bit<BF>(wa, A);
-        decode_1bit<BF>(wb, B8);
-      } else {
-        uint2 wa = make_uint2(0u, 0u), wb = make_uint2(0u, 0u);
-        if (ra < n_rows) {
-          wa = __ldg(reinterpret_cast<const uint2*>(codes + ra * crow + 32 * g) + q);
-          sa = __half2float(__ushort_as_half(__ldg(scales + static_cast<int64_t>(ra) * G + g)));
-        }
-        if (rb < n_rows) {
-          wb = __ldg(reinterpret_cast<const uint2*>(codes + rb * crow + 32 * g) + q);
-          sb = __half2float(__ushort_as_half(__ldg(scales + static_cast<int64_t>(rb) * G + g)));
-        }
-        decode_tern<BF>(wa.x, A);
-        decode_tern<BF>(wa.y, A + 8);
-        decode_tern<BF>(wb.x, B8);
-        decode_tern<BF>(wb.y, B8 + 8);
       }
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      if (ok && !lbdev::mbar_wait(&full[s], ph)) ok = false;
+      ok = __all_sync(0xffffffffu, ok);
+      // ---- the stage's codes and scales -> registers, then the slot goes back to the producer
+      uint2 ca[GH], cb[GH];                                        // rows ia / ia + 8, my 4 groups
+      if (ok) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mma16816<BF>(d, A[2 * i], B8[2 * i], A[2 * i + 1], B8[2 * i + 1], bx[2 * i], bx[2 * i + 1]);
-      acc[t][0] = fmaf(sa, d[0] - cc[0], acc[t][0]);
-      acc[t][1] = fmaf(sa, d[1] - cc[1], acc[t][1]);
-      acc[t][2] = fmaf(sb, d[2] - cc[2], acc[t][2]);
-      acc[t][3] = fmaf(sb, d[3] - cc[3], acc[t][3]);
+        for (int j = 0; j < GH; ++j) {
+          if (FMT == 1) {
+            const uint32_t o = slot + (pcode ^ (static_cast<uint32_t>(j) << 4));
+            ca[j] = make_uint2(ldsv32(o), 0u);
+            cb[j] = make_uint2(ldsv32(o + 1024), 0u);
+          } else {
+            const uint32_t o = slot + (pcode ^ (static_cast<uint32_t>(j) << 5));
+            ca[j] = ldsv64(o);
+            cb[j] = ldsv64(o + 1024);
+          }
+        }
+        if (a.scales_tma) {
+          const uint2 va = ldsv64(slot + sc_off), vb = ldsv64(slot + sc_off + 128);
+          const float2 a01 = __half22float2(*reinterpret_cast<const __half2*>(&va.x));
+          const float2 a23 = __half22float2(*reinterpret_cast<const __half2*>(&va.y));
+          const float2 b01 = __half22float2(*reinterpret_cast<const __half2*>(&vb.x));
+          const float2 b23 = __half22float2(*reinterpret_cast<const __half2*>(&vb.y));
+          sa[0] = a01.x; sa[1] = a01.y; sa[2] = a23.x; sa[3] = a23.y;
+          sb[0] = b01.x; sb[1] = b01.y; sb[2] = b23.x; sb[3] = b23.y;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) lbdev::mbar_arrive(&empty[s]);               // slot s released by this warp
+      if (++s == L::stages) { s = 0; ph ^= 1u; }
+
+      if (ok && cnt > 0) {
+        const uint32_t xbase = xs_lane + static_cast<uint32_t>(g0 * L::xgroup);
+        const uint32_t cbase = cn_q + static_cast<uint32_t>(g0 * 64);
+        // one group j (single accumulator chain); used for a ragged last stage
+        auto one_group = [&](int j) {
+          Word1 w1a = prep1(ca[j].x), w1b = prep1(cb[j].x);
+          Word2 wla = prep2(ca[j].x), wha = prep2(ca[j].y), wlb = prep2(cb[j].x), whb = prep2(cb[j].y);
+          const float4 cn = lds128f(cbase + j * 64);
+          uint4 bx[4];
+#pragma unroll
+          for (int iq = 0; iq < 4; ++iq) bx[iq] = lds128(xbase + j * L::xgroup + iq * (L::xgroup / 4));
+          float d[4];
+#define LB_ONE(I)                                                                                          \
+  {                                                                                                        \
+    const uint32_t blo = (I) % 2 == 0 ? bx[(I) / 2].x : bx[(I) / 2].z;                                      \
+    const uint32_t bhi = (I) % 2 == 0 ? bx[(I) / 2].y : bx[(I) / 2].w;                                      \
+    const uint32_t e0 = areg<FMT, 2 * (I)>(w1a, wla, wha, M), e1 = areg<FMT, 2 * (I)>(w1b, wlb, whb, M);      \
+    const uint32_t e2 = areg<FMT, 2 * (I) + 1>(w1a, wla, wha, M), e3 = areg<FMT, 2 * (I) + 1>(w1b, wlb, whb, M); \
+    if ((I) == 0) mma_c4(d, e0, e1, e2, e3, blo, bhi, cn);                                                 \
+    else mma_acc(d, e0, e1, e2, e3, blo, bhi);                                                             \
+  }
+          LB_ONE(0) LB_ONE(1) LB_ONE(2) LB_ONE(3) LB_ONE(4) LB_ONE(5) LB_ONE(6) LB_ONE(7)
+#undef LB_ONE
+          acc[0] = fmaf(sa[j], d[0], acc[0]);
+          acc[1] = fmaf(sa[j], d[1], acc[1]);
+          acc[2] = fmaf(sb[j], d[2], acc[2]);
+          acc[3] = fmaf(sb[j], d[3], acc[3]);
+        };
+        if (cnt == GH) {
+          // full stage: two pairs of groups, two independent accumulator chains per pair
+#pragma unroll
+          for (int jp = 0; jp < GH; jp += 2) {
+            Word1 w1a0 = prep1(ca[jp].x), w1b0 = prep1(cb[jp].x), w1a1 = prep1(ca[jp + 1].x), w1b1 = prep1(cb[jp + 1].x);
+            Word2 la0 = prep2(ca[jp].x), ha0 = prep2(ca[jp].y), lb0 = prep2(cb[jp].x), hb0 = prep2(cb[jp].y);
+            Word2 la1 = prep2(ca[jp + 1].x), ha1 = prep2(ca[jp + 1].y), lb1 = prep2(cb[jp + 1].x), hb1 = prep2(cb[jp + 1].y);
+            const float4 cn0 = lds128f(cbase + jp * 64), cn1 = lds128f(cbase + (jp + 1) * 64);
+            uint4 bx0[4], bx1[4];
+#pragma unroll
+            for (int iq = 0; iq < 4; ++iq) {
+              bx0[iq] = lds128(xbase + jp * L::xgroup + iq * (L::xgroup / 4));
+              bx1[iq] = lds128(xbase + (jp + 1) * L::xgroup + iq * (L::xgroup / 4));
+            }
+            float d0[4], d1[4];
+#define LB_PAIR(I)                                                                                         \
+  {                                                                                                        \
+    const uint32_t b0lo = (I) % 2 == 0 ? bx0[(I) / 2].x : bx0[(I) / 2].z;                                   \
+    const uint32_t b0hi = (I) % 2 == 0 ? bx0[(I) / 2].y : bx0[(I) / 2].w;                                   \
+    const uint32_t b1lo = (I) % 2 == 0 ? bx1[(I) / 2].x : bx1[(I) / 2].z;                                   \
+    const uint32_t b1hi = (I) % 2 == 0 ? bx1[(I) / 2].y : bx1[(I) / 2].w;                                   \
+    const uint32_t e00 = areg<FMT, 2 * (I)>(w1a0, la0, ha0, M), e01 = areg<FMT, 2 * (I)>(w1b0, lb0, hb0, M);  \
+    const uint32_t e02 = areg<FMT, 2 * (I) + 1>(w1a0, la0, ha0, M);                                         \
+    const uint32_t e03 = areg<FMT, 2 * (I) + 1>(w1b0, lb0, hb0, M);                                         \
+    const uint32_t e10 = areg<FMT, 2 * (I)>(w1a1, la1, ha1, M), e11 = areg<FMT, 2 * (I)>(w1b1, lb1, hb1, M);  \
+    const uint32_t e12 = areg<FMT, 2 * (I) + 1>(w1a1, la1, ha1, M);                                         \
+    const uint32_t e13 = areg<FMT, 2 * (I) + 1>(w1b1, lb1, hb1, M);                                         \
+    if ((I) == 0) {                                                                                        \
+      mma_c4(d0, e00, e01, e02, e03, b0lo, b0hi, cn0);                                                     \
+      mma_c4(d1, e10, e11, e12, e13, b1lo, b1hi, cn1);                                                     \
+    } else {                                                                                               \
+      mma_acc(d0, e00, e01, e02, e03, b0lo, b0hi);                                                         \
+      mma_acc(d1, e10, e11, e12, e13, b1lo, b1hi);                                                         \
+    }                                                                                                      \
+  }
+            LB_PAIR(0) LB_PAIR(1) LB_PAIR(2) LB_PAIR(3) LB_PAIR(4) LB_PAIR(5) LB_PAIR(6) LB_PAIR(7)
+#undef LB_PAIR
+            acc[0] = fmaf(sa[jp], d0[0], acc[0]);
+            acc[1] = fmaf(sa[jp], d0[1], acc[1]);
+            acc[2] = fmaf(sb[jp], d0[2], acc[2]);
+            acc[3] = fmaf(sb[jp], d0[3], acc[3]);
+            acc[0] = fmaf(sa[jp + 1], d1[0], acc[0]);
+            acc[1] = fmaf(sa[jp + 1], d1[1], acc[1]);
+            acc[2] = fmaf(sb[jp + 1], d1[2], acc[2]);
+            acc[3] = fmaf(sb[jp + 1], d1[3], acc[3]);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < GH; ++j)
+            if (j < cnt) one_group(j);
+        }
+      }
+
+      if (++cstage == nst) {
+        cstage = 0;
+        // ---- row block done: the two halves meet in shared memory (double-buffered by row block)
+        float* red = reinterpret_cast<float*>(sm + L::red) + (i_rb & 1) * ROWS * 8;
+        if (half == 1) {
+          red[ia * 8 + c0col] = acc[0];
+          red[ia * 8 + c1col] = acc[1];
+          red[(ia + 8) * 8 + c0col] = acc[2];
+          red[(ia + 8) * 8 + c1col] = acc[3];
+        }
+        if (st == total_st - 1) griddep_launch();
+        consumer_sync();
+        if (half == 0) {
+          const float v0 = (acc[0] + red[ia * 8 + c0col]) * f0;
+          const float v1 = (acc[1] + red[ia * 8 + c1col]) * f1;
+          const float v2 = (acc[2] + red[(ia + 8) * 8 + c0col]) * f0;
+          const float v3 = (acc[3] + red[(ia + 8) * 8 + c1col]) * f1;
+          if (a.S == 1) {
+            const int row_a = rb * ROWS + ia, row_b = row_a + 8;
+            auto put = [&](int row, int col, float v) {
+              if (row < a.n && col < a.batch)
+                a.y[static_cast<int64_t>(col) * a.n + row] =
+                    XBF ? __bfloat16_as_ushort(__float2bfloat16_rn(v)) : __half_as_ushort(__float2half_rn(v));
+            };
+            put(row_a, c0col, v0);
+            put(row_a, c1col, v1);
+            put(row_b, c0col, v2);
+            put(row_b, c1col, v3);
+          } else {
+            red[ia * 8 + c0col] = v0;                              // this CTA's partial, in output units
+            red[ia * 8 + c1col] = v1;
+            red[(ia + 8) * 8 + c0col] = v2;
+            red[(ia + 8) * 8 + c1col] = v3;
+          }
+        }
+        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+        ++i_rb;
+      }
     }
   }
 
-  // ---- reduce the four warps' K slices and store y (column c = 2q + {0,1}, rows ra / rb)
-  __shared__ float red[4][T][4][32];
-#pragma unroll
-  for (int t = 0; t < T; ++t)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) red[warp][t][e][lane] = acc[t][e];
-  __syncthreads();
-  const float mul = FMT == 1 ? 2.f : 1.f;
-  for (int idx = threadIdx.x; idx < T * 4 * 32; idx += blockDim.x) {
-    const int t = idx / 128, e = (idx / 32) & 3, l = idx & 31;
-    const float v = (red[0][t][e][l] + red[1][t][e][l] + red[2][t][e][l] + red[3][t][e][l]) * mul;
-    const int rr = l >> 2, qq = l & 3;
-    const int row = row0 + 16 * t + rr + ((e & 2) ? 8 : 0);
-    const int col = 2 * qq + (e & 1);
-    if (row < n_rows && col < batch) y[static_cast<int64_t>(col) * n_rows + row] = from_f32<BF>(v);
+  if (a.S > 1) {
+    // one row block per cluster: the S K-chunks' partial sums meet in distributed shared memory;
+    // every thread of every CTA (producer warp included) takes part in both cluster barriers
+    cluster_sync();
+    if (warp < NW) {
+      const int rb = static_cast<int>(blockIdx.y);
+      const int per = (ROWS + a.S - 1) / a.S;
+      const int lo = static_cast<int>(rank) * per, hi = min(ROWS, lo + per);
+      const uint32_t red = lbdev::smem_u32(sm + L::red);
+      for (int e = threadIdx.x; e < (hi - lo) * a.batch; e += NW * 32) {
+        const int lrow = lo + e / a.batch, col = e % a.batch;
+        const int row = rb * ROWS + lrow;
+        float v = 0.f;
+        for (int p = 0; p < a.S; ++p) v += ld_dsmem(red + (lrow * 8 + col) * 4, static_cast<uint32_t>(p));
+        if (row < a.n)
+          a.y[static_cast<int64_t>(col) * a.n + row] =
+              XBF ? __bfloat16_as_ushort(__float2bfloat16_rn(v)) : __half_as_ushort(__float2half_rn(v));
+      }
+    }
+    cluster_sync();
   }
+  if (!ok) atomicOr(a.err, lb::kErrGemmTimeout);
 }
 
-template <int FMT, bool BF>
+// ----------------------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+int pad_batch(int b) { return b <= 1 ? 1 : b <= 2 ? 2 : b <= 4 ? 4 : 8; }
+
+// Split of K across a cluster (S CTAs, chunk of gpc groups) from a simple time model: every CTA
+// pays a fixed cost (launch ramp, x prologue, first TMA latency; more with a cluster reduction),
+// then streams its row blocks x groups at the per-SM share of HBM bandwidth.
+struct Plan {
+  int S, gpc;
+};
+template <int FMT, int BP>
+Plan plan_split(int G, int row_blocks, int sms) {
+  using L = Layout<FMT, BP>;
+  const double t_group = 16384.0 * (FmtTraits<FMT>::gbytes + 2) / 128.0 / 40.0;   // ns per 128x128 tile
+  Plan best{0, 0};
+  double best_t = 1e30;
+  for (int s_try = 1; s_try <= kMaxCluster; ++s_try) {
+    const int per = (G + s_try - 1) / s_try;
+    const int g_try = s_try == 1 ? G : (per + GS - 1) / GS * GS;
+    const int s_eff = (G + g_try - 1) / g_try;
+    if (s_eff != s_try) continue;
+    if (L::total(g_try) > kSmemMax) continue;
+    double t;
+    if (s_eff == 1) {
+      const int per_cta = (row_blocks + sms - 1) / sms;
+      t = 2500.0 + per_cta * g_try * t_group;
+    } else {
+      const int clusters = max(1, sms / s_eff);
+      const int waves = (row_blocks + clusters - 1) / clusters;
+      t = waves * (3000.0 + g_try * t_group);
+    }
+    if (t < best_t * 0.999) { best_t = t; best = Plan{s_eff, g_try}; }
+  }
+  return best;
+}
+
+template <int FMT, bool XBF, int BP>
 lb_status launch_t(const lb_weight& W, const uint16_t* x, int batch, uint16_t* y, cudaStream_t st) {
-  const int n = static_cast<int>(W.n), k = static_cast<int>(W.k);
+  using L = Layout<FMT, BP>;
+  const int n = static_cast<int>(W.n), k = static_cast<int>(W.k), G = k / lb::kGroup;
+  const int gbytes = FmtTraits<FMT>::gbytes;
   const int sms = lb::sm_count();
-  int T = 1;
-  if ((n + 63) / 64 >= 2 * sms) T = 4;
-  else if ((n + 31) / 32 >= 2 * sms) T = 2;
-  const int rows = 16 * T;
-  const dim3 grid((n + rows - 1) / rows);
-  if (T == 4) gemv_mma_kernel<FMT, BF, 4><<<grid, 128, 0, st>>>(W.codes, W.scales, x, y, n, k, batch);
-  else if (T == 2) gemv_mma_kernel<FMT, BF, 2><<<grid, 128, 0, st>>>(W.codes, W.scales, x, y, n, k, batch);
-  else gemv_mma_kernel<FMT, BF, 1><<<grid, 128, 0, st>>>(W.codes, W.scales, x, y, n, k, batch);
-  cudaError_t e = cudaGetLastError();
+  const int row_blocks = (n + ROWS - 1) / ROWS;
+  const Plan plan = plan_split<FMT, BP>(G, row_blocks, sms);
+  if (plan.S == 0) return lb::fail(LB_ERR_UNSUPPORTED, "lb_gemv: K = %d too long for batch %d", k, batch);
+
+  Args args;
+  memset(&args, 0, sizeof(args));
+  args.scales_tma = (G % 8 == 0) ? 1 : 0;                          // scales row stride: 16-byte multiple
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return lb::fail(LB_ERR_CUDA, "lb_gemv: cuTensorMapEncodeTiled unavailable");
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k) * gbytes / 128, static_cast<cuuint64_t>(n)};
+    const cuuint64_t strides[1] = {dims[0]};
+    const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(ROWS)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(&args.tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(W.codes), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return lb::fail(LB_ERR_CUDA, "lb_gemv: codes tensor map (CUresult %d)", static_cast<int>(r));
+  }
+  if (args.scales_tma) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(G), static_cast<cuuint64_t>(n)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(G) * 2};
+    const cuuint32_t box[2] = {8, static_cast<cuuint32_t>(ROWS)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(&args.tm_scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t*>(W.scales), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return lb::fail(LB_ERR_CUDA, "lb_gemv: scales tensor map (CUresult %d)", static_cast<int>(r));
+  }
+  args.scales = W.scales;
+  args.x = x;
+  args.y = y;
+  args.err = lb::device_error_word();
+  if (!args.err) return lb::fail(LB_ERR_CUDA, "lb_gemv: device error word unavailable");
+  args.n = n;
+  args.k = k;
+  args.batch = batch;
+  args.G = G;
+  args.S = plan.S;
+  args.gpc = plan.gpc;
+  args.row_blocks = row_blocks;
+
+  const int smem = L::total(plan.gpc);
+  {
+    static std::mutex mu;
+    static bool done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(mu);
+    if (dev < 0 || dev >= 64 || !done[dev]) {
+      cudaError_t e = cudaFuncSetAttribute(gemv_kernel<FMT, XBF, BP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kSmemMax);
+      if (e != cudaSuccess) return lb::cuda_fail(e, "lb_gemv: shared memory attribute");
+      if (dev >= 0 && dev < 64) done[dev] = true;
+    }
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(plan.S, plan.S > 1 ? row_blocks : min(row_blocks, sms), 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attrs[2];
+  int na = 0;
+  attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  if (plan.S > 1) {
+    attrs[na].id = cudaLaunchAttributeClusterDimension;
+    attrs[na].val.clusterDim.x = plan.S;
+    attrs[na].val.clusterDim.y = 1;
+    attrs[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = na;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_kernel<FMT, XBF, BP>, args);
   if (e != cudaSuccess) return lb::cuda_fail(e, "lb_gemv: launch");
   return LB_OK;
+}
+
+template <int FMT, bool XBF>
+lb_status launch_b(const lb_weight& W, const uint16_t* x, int batch, uint16_t* y, cudaStream_t st) {
+  switch (pad_batch(batch)) {
+    case 1: return launch_t<FMT, XBF, 1>(W, x, batch, y, st);
+    case 2: return launch_t<FMT, XBF, 2>(W, x, batch, y, st);
+    case 4: return launch_t<FMT, XBF, 4>(W, x, batch, y, st);
+    default: return launch_t<FMT, XBF, 8>(W, x, batch, y, st);
+  }
 }
 
 }  // namespace
@@ -274,8 +749,8 @@ lb_status launch_gemv(const lb_weight& W, const void* x, int xdt, int batch, voi
   uint16_t* ys = static_cast<uint16_t*>(y);
   const bool bf = xdt == LB_BF16;
   if (W.fmt == LB_FMT_1BIT_G128)
-    return bf ? launch_t<1, true>(W, xs, batch, ys, st) : launch_t<1, false>(W, xs, batch, ys, st);
-  return bf ? launch_t<2, true>(W, xs, batch, ys, st) : launch_t<2, false>(W, xs, batch, ys, st);
+    return bf ? launch_b<1, true>(W, xs, batch, ys, st) : launch_b<1, false>(W, xs, batch, ys, st);
+  return bf ? launch_b<2, true>(W, xs, batch, ys, st) : launch_b<2, false>(W, xs, batch, ys, st);
 }
 
 }  // namespace lb
