@@ -189,6 +189,20 @@ lb_status lb_gemm(const lb_weight* W, const void* x, int xdt, int64_t m, void* y
   return lb::launch_gemm(*W, x, xdt, m, y, ydt, workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 
+lb_status lb_gemm_noalloc(const lb_weight* W, const void* x, int xdt, int64_t m, void* y, int ydt,
+                          lb_stream stream) {
+  lb_status s = check_weight(W);
+  if (s != LB_OK) return s;
+  if (!x || !y) return fail(LB_ERR_NULL, "x and y must be non-NULL");
+  if (!valid_dtype(xdt) || !valid_dtype(ydt)) return fail(LB_ERR_DTYPE, "unknown dtype (x %d, y %d)", xdt, ydt);
+  if (m < 1 || m > (int64_t(1) << 24)) return fail(LB_ERR_SHAPE, "m must be in [1, 2^24] (got %lld)", (long long)m);
+  if (W->n % 16) return fail(LB_ERR_SHAPE, "lb_gemm_noalloc needs n %% 16 == 0 (got %lld)", (long long)W->n);
+  if (W->fmt != LB_FMT_TERNARY_G128)
+    return fail(LB_ERR_UNSUPPORTED, "lb_gemm_noalloc implements the ternary format only");
+  if (!lb::aligned16(x) || !lb::aligned16(y)) return fail(LB_ERR_ALIGN, "x and y must be 16-byte aligned");
+  return lb::launch_gemm_noalloc(*W, x, xdt, m, y, ydt, reinterpret_cast<cudaStream_t>(stream));
+}
+
 lb_status lb_device_error(uint32_t* word, int clear) {
   if (!word) return fail(LB_ERR_NULL, "word is NULL");
   cudaError_t e = cudaDeviceSynchronize();

@@ -34,6 +34,8 @@ lb_status launch_gemv(const lb_weight& W, const void* x, int xdt, int batch, voi
 size_t gemm_workspace_bytes(int64_t m, int64_t k);
 lb_status launch_gemm(const lb_weight& W, const void* x, int xdt, int64_t m, void* y, int ydt,
                       void* ws, cudaStream_t st);
+lb_status launch_gemm_noalloc(const lb_weight& W, const void* x, int xdt, int64_t m, void* y, int ydt,
+                              cudaStream_t st);
 
 // Pack validation bits reported by the pack kernels.
 constexpr uint32_t kPackNonFinite = 1u;

@@ -269,7 +269,45 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+// Library-owned staging for lb_gemm_noalloc: callers that cannot allocate get the activation tiles
+// staged here instead of in a workspace of their own.  Every call rewrites every byte it later
+// reads (the prologue writes whole padded tiles), so the array never needs clearing; concurrent
+// calls would share it and must be serialised by the caller.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[LB_GEMM_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[64] = {};
+}  // namespace
+
 namespace lb {
+
+lb_status launch_gemm_noalloc(const lb_weight& W, const void* x, int xdt, int64_t m, void* y, int ydt,
+                              cudaStream_t st) {
+  const size_t need = gemm_workspace_bytes(m, W.k);
+  if (need > LB_GEMM_NOALLOC_SCRATCH_BYTES)
+    return fail(LB_ERR_WORKSPACE, "lb_gemm_noalloc: m = %lld, k = %lld needs %zu bytes of staging, more than the "
+                "%zu-byte library scratch", (long long)m, (long long)W.k, need,
+                static_cast<size_t>(LB_GEMM_NOALLOC_SCRATCH_BYTES));
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "lb_gemm_noalloc: cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(LB_ERR_UNSUPPORTED, "lb_gemm_noalloc: device index %d", dev);
+  void* ptr = nullptr;
+  {
+    // first call on this device (with it current): the host-side symbol is only a stand-in, the
+    // kernels need the array's device address
+    std::lock_guard<std::mutex> lk(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+      if (e != cudaSuccess) return cuda_fail(e, "lb_gemm_noalloc: cudaGetSymbolAddress");
+      g_noalloc_ptr[dev] = p;
+    }
+    ptr = g_noalloc_ptr[dev];
+  }
+  return launch_gemm(W, x, xdt, m, y, ydt, ptr, st);
+}
 
 size_t gemm_workspace_bytes(int64_t m, int64_t k) {
   const int64_t mpad = (m + BM - 1) / BM * BM;

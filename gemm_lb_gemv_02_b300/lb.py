@@ -29,7 +29,9 @@ STATUS_NAMES = {0: "LB_OK", 1: "LB_ERR_NULL", 2: "LB_ERR_SHAPE", 3: "LB_ERR_ALIG
 
 # Symbols declared in include/lb.h (checked by the tests against the header and the library).
 EXPORTED = ("lb_status_string", "lb_last_error", "lb_version", "lb_packed_bytes", "lb_pack_1bit",
-            "lb_pack_ternary", "lb_gemv", "lb_gemm_workspace_bytes", "lb_gemm", "lb_device_error")
+            "lb_pack_ternary", "lb_gemv", "lb_gemm_workspace_bytes", "lb_gemm", "lb_device_error",
+            "lb_gemm_noalloc")
+LB_GEMM_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class LBError(RuntimeError):
@@ -62,6 +64,7 @@ def _load():
         "lb_gemm_workspace_bytes": ([i64, i64, i64, i32, sz_p], i32),
         "lb_gemm": ([ctypes.POINTER(lb_weight), vp, i32, i64, vp, i32, vp, ctypes.c_size_t, vp], i32),
         "lb_device_error": ([ctypes.POINTER(ctypes.c_uint32), i32], i32),
+        "lb_gemm_noalloc": ([ctypes.POINTER(lb_weight), vp, i32, i64, vp, i32, vp], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -145,6 +148,11 @@ def lb_gemm(W: lb_weight, x, xdt: int, m: int, y, ydt: int, workspace, workspace
             stream=None) -> None:
     _check(_lib.lb_gemm(ctypes.byref(W), _ptr(x), xdt, m, _ptr(y), ydt, _ptr(workspace), workspace_bytes,
                         _stream(stream)), "lb_gemm")
+
+
+def lb_gemm_noalloc(W: lb_weight, x, xdt: int, m: int, y, ydt: int, stream=None) -> None:
+    """lb_gemm without a workspace: the library stages activations in its own static scratch."""
+    _check(_lib.lb_gemm_noalloc(ctypes.byref(W), _ptr(x), xdt, m, _ptr(y), ydt, _stream(stream)), "lb_gemm_noalloc")
 
 
 def lb_device_error(clear: bool = False) -> int:

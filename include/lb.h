@@ -167,6 +167,35 @@ lb_status lb_gemm(const lb_weight* W, const void* x, int xdt, int64_t m, void* y
  */
 lb_status lb_device_error(uint32_t* word, int clear);
 
+/* Size of the library-owned scratch used by lb_gemm_noalloc (8 MiB). */
+#define LB_GEMM_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+
+/*
+ * lb_gemm without a caller-provided workspace and without any allocation.  (The pages describe
+ * no such call: it exists for callers of this library that cannot allocate device memory.)
+ *
+ * Some callers cannot hand lb_gemm a workspace: plug-in style hosts that pass a kernel only its
+ * input and output buffers and give it no allocator, and serving loops that must not call
+ * cudaMalloc because it can synchronise the device and stall every other stream.  This entry point
+ * computes exactly what lb_gemm computes, with the same kernels, but keeps the activation staging
+ * in a scratch array that the library itself defines at file scope in device memory
+ * (LB_GEMM_NOALLOC_SCRATCH_BYTES; every GPU that loads the library holds it until the process
+ * exits).  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Arguments, layout, dtypes and error codes are those of lb_gemm, without the workspace pair.
+ * Additionally returns LB_ERR_WORKSPACE, before launching anything, when the staging the call
+ * needs (lb_gemm_workspace_bytes(m, n, k, xdt)) exceeds LB_GEMM_NOALLOC_SCRATCH_BYTES.
+ *
+ * The first call on a device looks up the device address of the scratch array with
+ * cudaGetSymbolAddress (with that device current) and caches it; make that first call before any
+ * stream capture.  All calls share the one array and it keeps the contents of the last call; each
+ * call rewrites every byte of it that it later reads, so nothing needs clearing between calls.
+ * Calls that overlap on the GPU (issued to different streams without ordering, or from several
+ * host threads at once) race on the array and give undefined results: serialise them.
+ */
+lb_status lb_gemm_noalloc(const lb_weight* W, const void* x, int xdt, int64_t m, void* y, int ydt,
+                          lb_stream stream);
+
 #ifdef __cplusplus
 }
 #endif
