@@ -211,11 +211,17 @@ class GemvSet:
 
 
 # ------------------------------------------------------------------------------------ measurements
-def measure_gemv_rows(lbt, peaks):
+def _want(name, sel):
+    return sel is None or any(name.startswith(p) for p in sel)
+
+
+def measure_gemv_rows(lbt, peaks, sel=None):
     rows = {}
     for key, batches in (("c1", (1,)), ("c3", (1, 4)), ("c4t", (1, 5)), ("c4b", (1, 5))):
         wl = synth.WORKLOADS[key]
         for b in batches:
+            if not _want(f"gemv_{key}_b{b}", sel):
+                continue
             gs = GemvSet(wl, b, lbt)
             steps = gs.copies * 2
             g = _graph(lambda: [gs.step() for _ in range(steps)])
@@ -232,8 +238,10 @@ def measure_gemv_rows(lbt, peaks):
     return rows
 
 
-def measure_pack_rows(lbt, peaks):
+def measure_pack_rows(lbt, peaks, sel=None):
     rows = {}
+    if not _want("pack", sel):
+        return rows
     wl = synth.WORKLOADS["c1"]
     w = synth.matrix_inputs(wl, 0)["w"]
     reps = 48                                            # 48 distinct 16 MB inputs > 4x L2
@@ -271,7 +279,9 @@ def measure_pack_rows(lbt, peaks):
     return rows
 
 
-def measure_gemm_row(lbt, peaks):
+def measure_gemm_row(lbt, peaks, sel=None):
+    if not _want("gemm_c5", sel):
+        return {}
     wl = synth.WORKLOADS["c5"]
     base = _pack_workload(wl, lbt)[0]
     x = synth.workload_activations(wl, 0, 512).cuda()
@@ -384,7 +394,7 @@ def run_ours(args, ws, rank, local):
 
     with ClockSampler(local) as clocks:
         # soak: keep the same load running for ~1.5 s so that the sampler sees it
-        t_end = time.perf_counter() + 1.5
+        t_end = time.perf_counter() + args.soak
         while time.perf_counter() < t_end:
             warm.replay()
         torch.cuda.synchronize()
@@ -436,22 +446,23 @@ def run_ours(args, ws, rank, local):
     del gs, warm, timed
     torch.cuda.empty_cache()
     rows = {}
-    if rank == 0 and not args.no_rows:
-        rows.update(measure_pack_rows(lbt, peaks))
-        rows.update(measure_gemv_rows(lbt, peaks))
-        rows.update(measure_gemm_row(lbt, peaks))
+    sel = None if args.rows == "all" else [r for r in args.rows.split(",") if r]
+    if rank == 0 and not args.no_rows and args.rows != "none":
+        rows.update(measure_pack_rows(lbt, peaks, sel))
+        rows.update(measure_gemv_rows(lbt, peaks, sel))
+        rows.update(measure_gemm_row(lbt, peaks, sel))
     assert lbl.lb_device_error(clear=True) == 0, "device error word set"
 
     if rank != 0:
         return
-    cpu_v, cpu_dt, cpu_passes = cpu_baseline(10.0)
+    cpu_v, cpu_dt, cpu_passes = cpu_baseline(args.cpu_seconds)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": _config(),
         "roofline": {"bound": "hbm", "achieved": round(per_rank_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(per_rank_gbs / peaks["hbm_gbs"], 4), "traffic": None,
-                     "kernel": "gemv_mma_kernel<ternary, f16> (7 launches per layer set)",
+                     "kernel": "gemv_kernel<ternary, f16 x, batch 1> (7 launches per layer set)",
                      "achieved_basis": "algorithmic bytes (packed codes + scales + x + y) per launch / "
                                        "(timed region / launches), CUDA events, so launch gaps count against it",
                      "peak_basis": f"{peaks['source']} STREAM-style copy bandwidth"},
@@ -477,6 +488,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row measurements")
+    ap.add_argument("--rows", default="all",
+                    help="comma-separated prefixes of the rows to measure (pack, gemv_c3, gemm_c5, ...), "
+                         "'all' or 'none'")
+    ap.add_argument("--soak", type=float, default=1.5,
+                    help="seconds of untimed load before the timed region (clock sampling)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline duration")
     args = ap.parse_args()
     ws, rank, local = _dist()
     if ws > 1:
