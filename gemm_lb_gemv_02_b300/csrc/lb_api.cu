@@ -161,6 +161,24 @@ lb_status lb_gemv(const lb_weight* W, const void* x, int xdt, int batch, void* y
   return lb::launch_gemv(*W, x, xdt, batch, y, reinterpret_cast<cudaStream_t>(stream));
 }
 
+lb_status lb_gemv_batched(const lb_gemv_problem* problems, int count, int xdt, int batch, lb_stream stream) {
+  if (!problems) return fail(LB_ERR_NULL, "problems is NULL");
+  if (count < 1 || count > LB_GEMV_BATCH_MAX)
+    return fail(LB_ERR_SHAPE, "count must be in [1, %d] (got %d)", LB_GEMV_BATCH_MAX, count);
+  if (!valid_dtype(xdt)) return fail(LB_ERR_DTYPE, "unknown activation dtype %d", xdt);
+  if (batch < 1 || batch > 8) return fail(LB_ERR_SHAPE, "batch must be in [1, 8] (got %d)", batch);
+  for (int i = 0; i < count; ++i) {
+    const lb_gemv_problem& pb = problems[i];
+    lb_status s = check_weight(&pb.W);
+    if (s != LB_OK) return s;
+    if (pb.W.fmt != problems[0].W.fmt)
+      return fail(LB_ERR_UNSUPPORTED, "problem %d: every problem of one call must have the same format", i);
+    if (!pb.x || !pb.y) return fail(LB_ERR_NULL, "problem %d: x and y must be non-NULL", i);
+    if (!lb::aligned16(pb.x) || !lb::aligned16(pb.y)) return fail(LB_ERR_ALIGN, "problem %d: x and y must be 16-byte aligned", i);
+  }
+  return lb::launch_gemv_batched(problems, count, xdt, batch, reinterpret_cast<cudaStream_t>(stream));
+}
+
 lb_status lb_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, int xdt, size_t* bytes) {
   if (!bytes) return fail(LB_ERR_NULL, "bytes is NULL");
   if (!valid_dtype(xdt)) return fail(LB_ERR_DTYPE, "unknown activation dtype %d", xdt);

@@ -179,18 +179,27 @@ __device__ __forceinline__ float4 lds128f(uint32_t a) {
   return v;
 }
 
-struct alignas(64) Args {
+constexpr int kMaxProblems = 8;           // GEMVs of one grouped launch
+
+// One GEMV of a launch.
+struct alignas(64) Prob {
   CUtensorMap tm_codes;       // codes plane as a 2-D u8 tensor {code bytes per row, n}, box 128 x 128
   CUtensorMap tm_scales;      // scales plane as a 2-D u16 tensor {G, n}, box 8 x 128 (if scales_tma)
   const uint16_t* scales;
   const uint16_t* x;
   uint16_t* y;
-  uint32_t* err;
-  int n, k, batch, G;
-  int S;           // CTAs per cluster along K (chunk = cluster rank)
+  int n, k, G;
   int gpc;         // groups per K chunk (a multiple of GS when S > 1)
   int row_blocks;
   int scales_tma;  // scales arrive in the stage through tm_scales
+  int unit0;       // first grid row (blockIdx.y) of this problem in a grouped launch
+};
+struct Args {
+  Prob p[kMaxProblems];
+  uint32_t* err;
+  int count;       // problems; 1 = one GEMV with persistent CTAs, > 1 = one CTA per row block
+  int batch;
+  int S;           // CTAs per cluster along K (chunk = cluster rank); 1 when count > 1
 };
 
 template <int FMT, int BP>
@@ -218,13 +227,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   uint64_t* empty = full + L::stages;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int pi = 0;                                                    // this CTA's problem
+  for (int i = 1; i < a.count; ++i)
+    if (static_cast<int>(blockIdx.y) >= a.p[i].unit0) pi = i;
+  const Prob& P = a.p[pi];
   const uint32_t rank = a.S > 1 ? cluster_rank() : 0u;
-  const int gpc = a.gpc;
+  const int gpc = P.gpc;
   const int g_begin = static_cast<int>(rank) * gpc;
-  const int ng = min(gpc, a.G - g_begin);                        // groups of this CTA's chunk (>= 1)
+  const int ng = min(gpc, P.G - g_begin);                        // groups of this CTA's chunk (>= 1)
   const int nst = (ng + GS - 1) / GS;                            // stages per row block
-  const int rb_stride = gridDim.y;
-  const int my_rbs = (a.row_blocks - static_cast<int>(blockIdx.y) + rb_stride - 1) / rb_stride;
+  // row blocks of this CTA: rb0, rb0 + rb_stride, ... (grouped launch: exactly one)
+  const int rb0 = static_cast<int>(blockIdx.y) - P.unit0;
+  const int rb_stride = a.count > 1 ? P.row_blocks : static_cast<int>(gridDim.y);
+  const int my_rbs = (P.row_blocks - rb0 + rb_stride - 1) / rb_stride;
   const int total_st = my_rbs * nst;
   bool ok = true;
 
@@ -241,20 +256,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   if (warp == NW) {
     // ======================= producer: weights do not depend on earlier kernels, so no wait
     if (lane == 0) {
-      lbdev::prefetch_tmap(&a.tm_codes);
-      if (a.scales_tma) lbdev::prefetch_tmap(&a.tm_scales);
-      const uint32_t bytes = static_cast<uint32_t>(FT::nb * kBox + (a.scales_tma ? kScaleBox : 0));
+      lbdev::prefetch_tmap(&P.tm_codes);
+      if (P.scales_tma) lbdev::prefetch_tmap(&P.tm_scales);
+      const uint32_t bytes = static_cast<uint32_t>(FT::nb * kBox + (P.scales_tma ? kScaleBox : 0));
       for (int st = 0; st < total_st; ++st) {
         const int s = st % L::stages;
         if (!lbdev::mbar_wait(&empty[s], static_cast<uint32_t>(((st / L::stages) & 1) ^ 1))) { ok = false; break; }
-        const int row0 = (static_cast<int>(blockIdx.y) + (st / nst) * rb_stride) * ROWS;
+        const int row0 = (rb0 + (st / nst) * rb_stride) * ROWS;
         const int g0 = g_begin + (st % nst) * GS;
         uint8_t* slot = sm + s * L::slot;
         lbdev::mbar_arrive_expect_tx(&full[s], bytes);
 #pragma unroll
         for (int b = 0; b < FT::nb; ++b)
-          lbdev::tma_load_2d(slot + b * kBox, &a.tm_codes, (g0 + b * (GS / FT::nb)) * FT::gbytes, row0, &full[s]);
-        if (a.scales_tma) lbdev::tma_load_2d(slot + FT::nb * kBox, &a.tm_scales, g0, row0, &full[s]);
+          lbdev::tma_load_2d(slot + b * kBox, &P.tm_codes, (g0 + b * (GS / FT::nb)) * FT::gbytes, row0, &full[s]);
+        if (P.scales_tma) lbdev::tma_load_2d(slot + FT::nb * kBox, &P.tm_scales, g0, row0, &full[s]);
       }
     }
     __syncwarp();
@@ -278,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         for (int i = 0; i < 16; ++i) X[i] = 0u;
         return false;
       }
-      const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(n) * a.k +
+      const uint4* src = reinterpret_cast<const uint4*>(P.x + static_cast<int64_t>(n) * P.k +
                                                         static_cast<int64_t>(g_begin + g) * 128 + 32 * qq);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -398,20 +413,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     uint32_t ph = 0;
 
     for (int st = 0; st < total_st; ++st) {
-      const int rb = static_cast<int>(blockIdx.y) + i_rb * rb_stride;
+      const int rb = rb0 + i_rb * rb_stride;
       const int g0 = cstage * GS + half * GH;                     // my first group, relative to g_begin
       const int cnt = min(GH, ng - g0);                           // my groups in this stage (may be <= 0)
       const uint32_t slot = sm32 + static_cast<uint32_t>(s * L::slot);
       float sa[GH], sb[GH];
-      if (!a.scales_tma) {                                        // fallback: scales from L2
+      if (!P.scales_tma) {                                        // fallback: scales from L2
         const int row_a = rb * ROWS + ia, row_b = row_a + 8;
 #pragma unroll
         for (int j = 0; j < GH; ++j) {
           sa[j] = 0.f; sb[j] = 0.f;
           if (j < cnt) {
             const int64_t g = g_begin + g0 + j;
-            if (row_a < a.n) sa[j] = __half2float(__ushort_as_half(__ldg(a.scales + static_cast<int64_t>(row_a) * a.G + g)));
-            if (row_b < a.n) sb[j] = __half2float(__ushort_as_half(__ldg(a.scales + static_cast<int64_t>(row_b) * a.G + g)));
+            if (row_a < P.n) sa[j] = __half2float(__ushort_as_half(__ldg(P.scales + static_cast<int64_t>(row_a) * P.G + g)));
+            if (row_b < P.n) sb[j] = __half2float(__ushort_as_half(__ldg(P.scales + static_cast<int64_t>(row_b) * P.G + g)));
           }
         }
       }
@@ -432,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             cb[j] = ldsv64(o + 1024);
           }
         }
-        if (a.scales_tma) {
+        if (P.scales_tma) {
           const uint2 va = ldsv64(slot + sc_off), vb = ldsv64(slot + sc_off + 128);
           const float2 a01 = __half22float2(*reinterpret_cast<const __half2*>(&va.x));
           const float2 a23 = __half22float2(*reinterpret_cast<const __half2*>(&va.y));
@@ -547,8 +562,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
           if (a.S == 1) {
             const int row_a = rb * ROWS + ia, row_b = row_a + 8;
             auto put = [&](int row, int col, float v) {
-              if (row < a.n && col < a.batch)
-                a.y[static_cast<int64_t>(col) * a.n + row] =
+              if (row < P.n && col < a.batch)
+                P.y[static_cast<int64_t>(col) * P.n + row] =
                     XBF ? __bfloat16_as_ushort(__float2bfloat16_rn(v)) : __half_as_ushort(__float2half_rn(v));
             };
             put(row_a, c0col, v0);
@@ -573,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     // every thread of every CTA (producer warp included) takes part in both cluster barriers
     cluster_sync();
     if (warp < NW) {
-      const int rb = static_cast<int>(blockIdx.y);
+      const int rb = rb0;
       const int per = (ROWS + a.S - 1) / a.S;
       const int lo = static_cast<int>(rank) * per, hi = min(ROWS, lo + per);
       const uint32_t red = lbdev::smem_u32(sm + L::red);
@@ -582,8 +597,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         const int row = rb * ROWS + lrow;
         float v = 0.f;
         for (int p = 0; p < a.S; ++p) v += ld_dsmem(red + (lrow * 8 + col) * 4, static_cast<uint32_t>(p));
-        if (row < a.n)
-          a.y[static_cast<int64_t>(col) * a.n + row] =
+        if (row < P.n)
+          P.y[static_cast<int64_t>(col) * P.n + row] =
               XBF ? __bfloat16_as_ushort(__float2bfloat16_rn(v)) : __half_as_ushort(__float2half_rn(v));
       }
     }
@@ -644,19 +659,13 @@ Plan plan_split(int G, int row_blocks, int sms) {
   return best;
 }
 
-template <int FMT, bool XBF, int BP>
-lb_status launch_t(const lb_weight& W, const uint16_t* x, int batch, uint16_t* y, cudaStream_t st) {
-  using L = Layout<FMT, BP>;
+// Tensor maps and sizes of one problem (gpc: groups per K chunk of the launch's split).
+template <int FMT>
+lb_status fill_prob(const lb_weight& W, const void* x, void* y, int gpc, Prob& pr) {
   const int n = static_cast<int>(W.n), k = static_cast<int>(W.k), G = k / lb::kGroup;
   const int gbytes = FmtTraits<FMT>::gbytes;
-  const int sms = lb::sm_count();
-  const int row_blocks = (n + ROWS - 1) / ROWS;
-  const Plan plan = plan_split<FMT, BP>(G, row_blocks, sms);
-  if (plan.S == 0) return lb::fail(LB_ERR_UNSUPPORTED, "lb_gemv: K = %d too long for batch %d", k, batch);
-
-  Args args;
-  memset(&args, 0, sizeof(args));
-  args.scales_tma = (G % 8 == 0) ? 1 : 0;                          // scales row stride: 16-byte multiple
+  memset(&pr, 0, sizeof(pr));
+  pr.scales_tma = (G % 8 == 0) ? 1 : 0;                            // scales row stride: 16-byte multiple
   EncodeTiledFn enc = encode_fn();
   if (!enc) return lb::fail(LB_ERR_CUDA, "lb_gemv: cuTensorMapEncodeTiled unavailable");
   {
@@ -664,35 +673,36 @@ lb_status launch_t(const lb_weight& W, const uint16_t* x, int batch, uint16_t* y
     const cuuint64_t strides[1] = {dims[0]};
     const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(ROWS)};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(&args.tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(W.codes), dims, strides,
+    CUresult r = enc(&pr.tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(W.codes), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return lb::fail(LB_ERR_CUDA, "lb_gemv: codes tensor map (CUresult %d)", static_cast<int>(r));
   }
-  if (args.scales_tma) {
+  if (pr.scales_tma) {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(G), static_cast<cuuint64_t>(n)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(G) * 2};
     const cuuint32_t box[2] = {8, static_cast<cuuint32_t>(ROWS)};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(&args.tm_scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t*>(W.scales), dims,
+    CUresult r = enc(&pr.tm_scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t*>(W.scales), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return lb::fail(LB_ERR_CUDA, "lb_gemv: scales tensor map (CUresult %d)", static_cast<int>(r));
   }
-  args.scales = W.scales;
-  args.x = x;
-  args.y = y;
+  pr.scales = W.scales;
+  pr.x = static_cast<const uint16_t*>(x);
+  pr.y = static_cast<uint16_t*>(y);
+  pr.n = n;
+  pr.k = k;
+  pr.G = G;
+  pr.gpc = gpc;
+  pr.row_blocks = (n + ROWS - 1) / ROWS;
+  return LB_OK;
+}
+
+template <int FMT, bool XBF, int BP>
+lb_status launch_args(Args& args, int grid_x, int grid_y, int smem, cudaStream_t st) {
   args.err = lb::device_error_word();
   if (!args.err) return lb::fail(LB_ERR_CUDA, "lb_gemv: device error word unavailable");
-  args.n = n;
-  args.k = k;
-  args.batch = batch;
-  args.G = G;
-  args.S = plan.S;
-  args.gpc = plan.gpc;
-  args.row_blocks = row_blocks;
-
-  const int smem = L::total(plan.gpc);
   {
     static std::mutex mu;
     static bool done[64] = {};
@@ -707,7 +717,7 @@ lb_status launch_t(const lb_weight& W, const uint16_t* x, int batch, uint16_t* y
     }
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(plan.S, plan.S > 1 ? row_blocks : min(row_blocks, sms), 1);
+  cfg.gridDim = dim3(grid_x, grid_y, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -716,9 +726,9 @@ lb_status launch_t(const lb_weight& W, const uint16_t* x, int batch, uint16_t* y
   attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attrs[na].val.programmaticStreamSerializationAllowed = 1;
   ++na;
-  if (plan.S > 1) {
+  if (args.S > 1) {
     attrs[na].id = cudaLaunchAttributeClusterDimension;
-    attrs[na].val.clusterDim.x = plan.S;
+    attrs[na].val.clusterDim.x = args.S;
     attrs[na].val.clusterDim.y = 1;
     attrs[na].val.clusterDim.z = 1;
     ++na;
@@ -730,6 +740,61 @@ lb_status launch_t(const lb_weight& W, const uint16_t* x, int batch, uint16_t* y
   return LB_OK;
 }
 
+// One GEMV: persistent CTAs over row blocks, K split across a cluster when that is faster.
+template <int FMT, bool XBF, int BP>
+lb_status launch_t(const lb_weight& W, const uint16_t* x, int batch, uint16_t* y, cudaStream_t st) {
+  using L = Layout<FMT, BP>;
+  const int k = static_cast<int>(W.k), G = k / lb::kGroup;
+  const int sms = lb::sm_count();
+  const int row_blocks = static_cast<int>((W.n + ROWS - 1) / ROWS);
+  const Plan plan = plan_split<FMT, BP>(G, row_blocks, sms);
+  if (plan.S == 0) return lb::fail(LB_ERR_UNSUPPORTED, "lb_gemv: K = %d too long for batch %d", k, batch);
+  static_assert(sizeof(Args) <= 4096, "kernel parameters");
+  Args args;
+  memset(&args, 0, sizeof(args));
+  lb_status s = fill_prob<FMT>(W, x, y, plan.gpc, args.p[0]);
+  if (s != LB_OK) return s;
+  args.count = 1;
+  args.batch = batch;
+  args.S = plan.S;
+  return launch_args<FMT, XBF, BP>(args, plan.S, plan.S > 1 ? row_blocks : min(row_blocks, sms),
+                                   L::total(plan.gpc), st);
+}
+
+// Several GEMVs in one launch: one CTA per (problem, row block), whole K per CTA.  Problems with
+// the longest K get the first grid rows, so that the slowest CTAs start first.
+template <int FMT, bool XBF, int BP>
+lb_status launch_many(const lb_gemv_problem* probs, int count, int batch, cudaStream_t st) {
+  using L = Layout<FMT, BP>;
+  int order[kMaxProblems];
+  for (int i = 0; i < count; ++i) order[i] = i;
+  for (int i = 1; i < count; ++i)                                  // stable insertion sort, K descending
+    for (int j = i; j > 0 && probs[order[j]].W.k > probs[order[j - 1]].W.k; --j) {
+      const int t = order[j];
+      order[j] = order[j - 1];
+      order[j - 1] = t;
+    }
+  Args args;
+  memset(&args, 0, sizeof(args));
+  int units = 0, smem = 0;
+  for (int i = 0; i < count; ++i) {
+    const lb_gemv_problem& pb = probs[order[i]];
+    const int G = static_cast<int>(pb.W.k / lb::kGroup);
+    if (L::total(G) > kSmemMax)
+      return lb::fail(LB_ERR_UNSUPPORTED, "lb_gemv_batched: K = %lld too long for one CTA at batch %d",
+                      static_cast<long long>(pb.W.k), batch);
+    lb_status s = fill_prob<FMT>(pb.W, pb.x, pb.y, G, args.p[i]);
+    if (s != LB_OK) return s;
+    args.p[i].unit0 = units;
+    units += args.p[i].row_blocks;
+    smem = max(smem, L::total(G));
+  }
+  args.count = count;
+  args.batch = batch;
+  args.S = 1;
+  return launch_args<FMT, XBF, BP>(args, 1, units, smem, st);
+}
+
 template <int FMT, bool XBF>
 lb_status launch_b(const lb_weight& W, const uint16_t* x, int batch, uint16_t* y, cudaStream_t st) {
   switch (pad_batch(batch)) {
@@ -737,6 +802,15 @@ lb_status launch_b(const lb_weight& W, const uint16_t* x, int batch, uint16_t* y
     case 2: return launch_t<FMT, XBF, 2>(W, x, batch, y, st);
     case 4: return launch_t<FMT, XBF, 4>(W, x, batch, y, st);
     default: return launch_t<FMT, XBF, 8>(W, x, batch, y, st);
+  }
+}
+template <int FMT, bool XBF>
+lb_status launch_mb(const lb_gemv_problem* probs, int count, int batch, cudaStream_t st) {
+  switch (pad_batch(batch)) {
+    case 1: return launch_many<FMT, XBF, 1>(probs, count, batch, st);
+    case 2: return launch_many<FMT, XBF, 2>(probs, count, batch, st);
+    case 4: return launch_many<FMT, XBF, 4>(probs, count, batch, st);
+    default: return launch_many<FMT, XBF, 8>(probs, count, batch, st);
   }
 }
 
@@ -751,6 +825,14 @@ lb_status launch_gemv(const lb_weight& W, const void* x, int xdt, int batch, voi
   if (W.fmt == LB_FMT_1BIT_G128)
     return bf ? launch_b<1, true>(W, xs, batch, ys, st) : launch_b<1, false>(W, xs, batch, ys, st);
   return bf ? launch_b<2, true>(W, xs, batch, ys, st) : launch_b<2, false>(W, xs, batch, ys, st);
+}
+
+lb_status launch_gemv_batched(const lb_gemv_problem* probs, int count, int xdt, int batch, cudaStream_t st) {
+  if (count > kMaxProblems) return fail(LB_ERR_SHAPE, "lb_gemv_batched: count %d > %d", count, kMaxProblems);
+  const bool bf = xdt == LB_BF16;
+  if (probs[0].W.fmt == LB_FMT_1BIT_G128)
+    return bf ? launch_mb<1, true>(probs, count, batch, st) : launch_mb<1, false>(probs, count, batch, st);
+  return bf ? launch_mb<2, true>(probs, count, batch, st) : launch_mb<2, false>(probs, count, batch, st);
 }
 
 }  // namespace lb

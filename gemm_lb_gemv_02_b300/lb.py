@@ -30,8 +30,9 @@ STATUS_NAMES = {0: "LB_OK", 1: "LB_ERR_NULL", 2: "LB_ERR_SHAPE", 3: "LB_ERR_ALIG
 # Symbols declared in include/lb.h (checked by the tests against the header and the library).
 EXPORTED = ("lb_status_string", "lb_last_error", "lb_version", "lb_packed_bytes", "lb_pack_1bit",
             "lb_pack_ternary", "lb_gemv", "lb_gemm_workspace_bytes", "lb_gemm", "lb_device_error",
-            "lb_gemm_noalloc")
+            "lb_gemm_noalloc", "lb_gemv_batched")
 LB_GEMM_NOALLOC_SCRATCH_BYTES = 8 << 20
+LB_GEMV_BATCH_MAX = 8
 
 
 class LBError(RuntimeError):
@@ -44,6 +45,10 @@ class LBError(RuntimeError):
 class lb_weight(ctypes.Structure):
     _fields_ = [("fmt", ctypes.c_int32), ("reserved", ctypes.c_int32), ("n", ctypes.c_int64),
                 ("k", ctypes.c_int64), ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p)]
+
+
+class lb_gemv_problem(ctypes.Structure):
+    _fields_ = [("W", lb_weight), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p)]
 
 
 def _load():
@@ -65,6 +70,7 @@ def _load():
         "lb_gemm": ([ctypes.POINTER(lb_weight), vp, i32, i64, vp, i32, vp, ctypes.c_size_t, vp], i32),
         "lb_device_error": ([ctypes.POINTER(ctypes.c_uint32), i32], i32),
         "lb_gemm_noalloc": ([ctypes.POINTER(lb_weight), vp, i32, i64, vp, i32, vp], i32),
+        "lb_gemv_batched": ([ctypes.POINTER(lb_gemv_problem), i32, i32, i32, vp], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -136,6 +142,14 @@ def make_weight(fmt: int, n: int, k: int, codes, scales) -> lb_weight:
 
 def lb_gemv(W: lb_weight, x, xdt: int, batch: int, y, stream=None) -> None:
     _check(_lib.lb_gemv(ctypes.byref(W), _ptr(x), xdt, batch, _ptr(y), _stream(stream)), "lb_gemv")
+
+
+def lb_gemv_batched(problems, xdt: int, batch: int, stream=None) -> None:
+    """problems: sequence of (lb_weight, x, y) triples (device tensors or addresses)."""
+    arr = (lb_gemv_problem * max(1, len(problems)))()
+    for i, (W, x, y) in enumerate(problems):
+        arr[i] = lb_gemv_problem(W, _ptr(x), _ptr(y))
+    _check(_lib.lb_gemv_batched(arr, len(problems), xdt, batch, _stream(stream)), "lb_gemv_batched")
 
 
 def lb_gemm_workspace_bytes(m: int, n: int, k: int, xdt: int) -> int:

@@ -69,6 +69,20 @@ def gemv(W: PackedWeight, x: torch.Tensor, y: torch.Tensor | None = None, stream
     return y
 
 
+def gemv_batched(problems, ys=None, stream=None) -> list:
+    """Several GEMVs in one launch: problems = [(PackedWeight, x)], every x [batch][k] of one dtype
+    and batch (x tensors may be shared).  Returns the outputs y [batch][n] (or fills `ys`)."""
+    assert problems
+    x0 = problems[0][1]
+    batch, dt = x0.shape[0], x0.dtype
+    if ys is None:
+        ys = [torch.empty(batch, W.n, dtype=dt, device=x.device) for W, x in problems]
+    for W, x in problems:
+        assert x.is_cuda and x.is_contiguous() and x.dim() == 2 and x.shape == (batch, W.k) and x.dtype == dt
+    lb.lb_gemv_batched([(W.struct(), x, y) for (W, x), y in zip(problems, ys)], dtype_code(dt), batch, stream)
+    return ys
+
+
 def gemm(W: PackedWeight, x: torch.Tensor, out_dtype: torch.dtype = torch.bfloat16,
          y: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Y[m][n] = X W^T for X [m][k]; output dtype out_dtype."""

@@ -134,6 +134,31 @@ lb_status lb_pack_ternary(const int8_t* t, const uint16_t* s_in, int64_t n, int6
  */
 lb_status lb_gemv(const lb_weight* W, const void* x, int xdt, int batch, void* y, lb_stream stream);
 
+/* One GEMV of a grouped call: y = W x with the layouts of lb_gemv (all pointers device, caller-owned). */
+typedef struct lb_gemv_problem {
+  lb_weight W;
+  const void* x;          /* [batch][W.k] of the call's xdt, 16-byte aligned */
+  void* y;                /* [batch][W.n] of the call's xdt, 16-byte aligned */
+} lb_gemv_problem;
+
+#define LB_GEMV_BATCH_MAX 8
+
+/*
+ * Several independent decode GEMVs in one launch (the matrices of one decoder layer that read the
+ * same activations, e.g. q / k / v or gate / up; 7minutos.es, "PrismML lanza Bonsai 27B", section
+ * "Rendimiento y decodificación especulativa DSpark": decode streams every weight once per token, so
+ * at small matrix sizes the fixed cost of a launch dominates).  Each problem computes exactly what
+ * lb_gemv computes for it; problems may differ in n, k, x and y (x buffers may be shared).
+ *
+ * problems : host array of `count` problems, 1 <= count <= LB_GEMV_BATCH_MAX, all of the same format.
+ * xdt      : LB_F16 or LB_BF16 for every x and y;  batch : 1 .. 8 for every problem.
+ * No y may overlap another problem's x or y.  Asynchronous on `stream`.  Errors (no launch):
+ * LB_ERR_NULL, LB_ERR_SHAPE (count or batch out of range, a bad n / k), LB_ERR_ALIGN, LB_ERR_DTYPE,
+ * LB_ERR_UNSUPPORTED (mixed formats, or a k too long for one CTA: k <= 44672 at batch 1, 24832 at
+ * batch 2, 13056 at batch 3-4, 6784 at batch 5-8), LB_ERR_CUDA if the launch fails.
+ */
+lb_status lb_gemv_batched(const lb_gemv_problem* problems, int count, int xdt, int batch, lb_stream stream);
+
 /*
  * Workspace bytes that lb_gemm needs for an m x k activation matrix of dtype `xdt` against an
  * n x k weight (0 means none is needed).  Pure host arithmetic.

@@ -95,3 +95,23 @@ def test_gemm_validation():
     assert _status(lb.lb_gemm, lb.make_weight(1, 256, 256, A16, A16), A16, lb.LB_BF16, 5, A16, lb.LB_BF16,
                    A16, need, 0) == "LB_ERR_UNSUPPORTED"
     assert _status(lb.lb_gemm, W, A16, 5, 5, A16, lb.LB_BF16, A16, need, 0) == "LB_ERR_DTYPE"
+
+
+def test_gemv_batched_validation():
+    W1 = lb.make_weight(lb.LB_FMT_1BIT_G128, 16, 128, A16, A16)
+    Wt = lb.make_weight(lb.LB_FMT_TERNARY_G128, 16, 128, A16, A16)
+    ok = (W1, A16, A16)
+    raw = lb.library().lb_gemv_batched
+    assert lb.lb_status_string(raw(None, 1, lb.LB_F16, 1, None)).startswith("LB_ERR_NULL")
+    assert _status(lb.lb_gemv_batched, [], lb.LB_F16, 1) == "LB_ERR_SHAPE"
+    assert _status(lb.lb_gemv_batched, [ok] * (lb.LB_GEMV_BATCH_MAX + 1), lb.LB_F16, 1) == "LB_ERR_SHAPE"
+    assert _status(lb.lb_gemv_batched, [ok], 9, 1) == "LB_ERR_DTYPE"
+    assert _status(lb.lb_gemv_batched, [ok], lb.LB_F16, 9) == "LB_ERR_SHAPE"
+    assert _status(lb.lb_gemv_batched, [ok, (Wt, A16, A16)], lb.LB_F16, 1) == "LB_ERR_UNSUPPORTED"
+    assert _status(lb.lb_gemv_batched, [ok, (W1, None, A16)], lb.LB_F16, 1) == "LB_ERR_NULL"
+    assert _status(lb.lb_gemv_batched, [ok, (W1, A16, MIS)], lb.LB_F16, 1) == "LB_ERR_ALIGN"
+    assert _status(lb.lb_gemv_batched, [ok, (lb.make_weight(1, 16, 130, A16, A16), A16, A16)], lb.LB_F16, 1) == "LB_ERR_SHAPE"
+    # one CTA holds the whole K of a problem: the documented limits
+    for batch, kmax in ((1, 44672), (2, 24832), (4, 13056), (8, 6784)):
+        long_w = lb.make_weight(lb.LB_FMT_1BIT_G128, 16, kmax + 128, A16, A16)
+        assert _status(lb.lb_gemv_batched, [(long_w, A16, A16)], lb.LB_F16, batch) == "LB_ERR_UNSUPPORTED"

@@ -41,7 +41,8 @@ def _run_guarded(pw, x):
 
 @pytest.mark.parametrize("fmt", ["1bit", "ternary"])
 @pytest.mark.parametrize("xdt", ["f16", "bf16"])
-@pytest.mark.parametrize("n,k", [(1, 128), (7, 256), (16, 128), (17, 640), (100, 384), (333, 1024), (1100, 512)])
+@pytest.mark.parametrize("n,k", [(1, 128), (7, 256), (16, 128), (17, 640), (100, 384), (333, 1024), (1100, 512),
+                                 (300, 2176), (37893, 384)])
 def test_gemv_small_shapes(fmt, xdt, n, k):
     pw, codes, scales = _packed(fmt, n, k, seed=n * 7 + k)
     for batch in (1, 2, 3, 5, 8):
@@ -121,3 +122,52 @@ def test_gemv_c3_lm_head(batch):
 @pytest.mark.parametrize("batch", [1, 5])
 def test_gemv_c4_layer_set(key, batch):
     _workload_check(key, batch, sample_rows=1500)
+
+
+@pytest.mark.parametrize("fmt", ["1bit", "ternary"])
+@pytest.mark.parametrize("xdt", ["f16", "bf16"])
+@pytest.mark.parametrize("batch", [1, 3, 8])
+def test_gemv_batched_mixed_shapes(fmt, xdt, batch):
+    """One grouped launch over problems of different n and k (ragged row blocks, partial stages,
+    group counts that are not multiples of 8), some sharing one x: each y matches the oracle and
+    nothing is written outside any y."""
+    shapes = [(300, 2176), (17, 640), (1100, 512), (129, 128), (2048, 1024)]
+    packed = [_packed(fmt, n, k, seed=n + 3 * k) for n, k in shapes]
+    xs = {k: synth.activations(batch, k, xdt, seed=k + batch).cuda() for _, k in shapes}
+    pad = 64
+    bufs, ys = [], []
+    for n, k in shapes:
+        buf = torch.full((batch * n + 2 * pad,), 12345, dtype=torch.int16, device="cuda")
+        bufs.append(buf)
+        ys.append(buf[pad:pad + batch * n].view(TDT[xdt]).view(batch, n))
+    tensors.gemv_batched([(pw, xs[k]) for (pw, _, _), (n, k) in zip(packed, shapes)], ys)
+    torch.cuda.synchronize()
+    for (pw, codes, scales), (n, k), y, buf in zip(packed, shapes, ys, bufs):
+        assert torch.all(buf[:pad] == 12345) and torch.all(buf[pad + batch * n:] == 12345), "write outside y"
+        y_ref, a = oracle_products(fmt, codes, scales, k, xs[k].cpu())
+        check_products(y, y_ref, a, f"batched {fmt} {xdt} n={n} k={k} batch={batch}")
+
+
+def test_gemv_batched_c2_layer_set_grouping():
+    """The 1.7B-class ternary layer set as a decoder layer issues it: [q, k, v] on one x, [o],
+    [gate, up] on one x, [down]; every output matches the oracle."""
+    wl = synth.WORKLOADS["c2"]
+    mats = {}
+    for i, mat in enumerate(wl.matrices):
+        inp = synth.matrix_inputs(wl, i)
+        mats[mat.name] = (tensors.pack_ternary(inp["t"].cuda(), inp["s"].cuda()), mat)
+    x_attn = synth.activations(1, 2048, "f16", seed=71).cuda()
+    x_o = synth.activations(1, 2048, "f16", seed=72).cuda()
+    x_ffn = synth.activations(1, 2048, "f16", seed=73).cuda()
+    x_down = synth.activations(1, 6144, "f16", seed=74).cuda()
+    groups = [[("q", x_attn), ("k", x_attn), ("v", x_attn)], [("o", x_o)], [("gate", x_ffn), ("up", x_ffn)],
+              [("down", x_down)]]
+    for grp in groups:
+        ys = tensors.gemv_batched([(mats[name][0], x) for name, x in grp])
+        torch.cuda.synchronize()
+        for (name, x), y in zip(grp, ys):
+            pw, mat = mats[name]
+            codes = u8(pw.codes).reshape(mat.n, -1)
+            scales = u16(pw.scales).reshape(mat.n, -1)
+            y_ref, a = oracle_products("ternary", codes, scales, mat.k, x.cpu())
+            check_products(y, y_ref, a, f"c2/{name} grouped")
