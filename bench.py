@@ -5,8 +5,10 @@
 Headline workload (one JSON line on stdout, rank 0): the ternary decode layer set of a 1.7B-class
 block (q, k, v, o 2048x2048; gate, up 6144x2048; down 2048x6144; codes iid {-1,0,+1} with
 p = (0.3, 0.4, 0.3); scales |N(0, 0.02)| in fp16; x fp16 N(0, 1); batch 1).  One step decodes one
-token through LAYERS distinct copies of that layer set (7 GEMV launches per copy), so the weights
-a step streams (~525 MB) exceed 4x the 126 MB L2 and every step reads them from HBM.  The K timed
+token through LAYERS distinct copies of that layer set, each issued the way a decoder layer issues
+it: [q, k, v] on one activation vector (one lb_gemv_batched launch), [o] (lb_gemv), [gate, up] on
+one vector (lb_gemv_batched), [down] (lb_gemv), i.e. 4 launches per copy.  The weights a step
+streams (~525 MB) exceed 4x the 126 MB L2, so every step reads them from HBM.  The K timed
 steps are one CUDA-graph replay, timed with CUDA events on the launching stream.
 
 ``value`` is the algorithmic packed-weight bandwidth (packed codes + scales + x + y bytes per step
@@ -183,26 +185,62 @@ def _time_graph(g, reps: int = 1) -> float:
     return e0.elapsed_time(e1) / reps
 
 
-class GemvSet:
-    """Rotating copies of a workload's matrices; one 'step' runs one GEMV per matrix per copy."""
+# How a decoder layer issues its matrices: each inner list is one launch (lb_gemv for one matrix,
+# lb_gemv_batched for several); the matrices of a launch read the same activations.
+LAYER_GROUPING = {
+    "c2": [["q", "k", "v"], ["o"], ["gate", "up"], ["down"]],
+    "c4t": [["q"], ["o"], ["gate", "up"], ["down"]],
+    "c4b": [["q"], ["o"], ["gate", "up"], ["down"]],
+}
 
-    def __init__(self, wl, batch, lbt, copies=None, layers_per_step=None):
+
+def grouping_of(wl, mode):
+    """mode: 'separate' (one launch per matrix), 'layer' (LAYER_GROUPING), 'one' (a single launch)."""
+    names = [m.name for m in wl.matrices]
+    if mode == "separate" or wl.key not in LAYER_GROUPING:
+        return [[i] for i in range(len(names))]
+    if mode == "one":
+        return [list(range(len(names)))]
+    return [[names.index(n) for n in grp] for grp in LAYER_GROUPING[wl.key]]
+
+
+class GemvSet:
+    """Rotating copies of a workload's matrices; one 'step' runs every matrix of one copy, issued as
+    the grouping says (matrices of one launch share the first one's activations)."""
+
+    def __init__(self, wl, batch, lbt, copies=None, layers_per_step=None, grouping="separate"):
         self.wl, self.batch, self.lbt = wl, batch, lbt
         base = _pack_workload(wl, lbt)
         per_copy = sum(_gemv_bytes(pw, batch) for pw in base)
         self.copies = copies or _copies_for(per_copy)
         self.sets = [base] + [[_clone(pw) for pw in base] for _ in range(self.copies - 1)]
         self.layers = layers_per_step or 1
-        self.x = [synth.workload_activations(wl, i, batch).cuda() for i in range(len(wl.matrices))]
+        self.groups = grouping_of(wl, grouping)
+        self.grouping = grouping
+        own = [synth.workload_activations(wl, i, batch).cuda() for i in range(len(wl.matrices))]
+        self.x = list(own)
+        for grp in self.groups:                  # same-K members of a launch share one vector
+            for i in grp:
+                if wl.matrices[i].k == wl.matrices[grp[0]].k:
+                    self.x[i] = own[grp[0]]
         self.y = [torch.empty(batch, m.n, dtype=self.x[i].dtype, device="cuda") for i, m in enumerate(wl.matrices)]
-        self.bytes_per_layer = per_copy
-        self.launches_per_layer = len(base)
+        self.bytes_per_layer = sum(_gemv_bytes(pw, batch) for pw in base) - sum(
+            2 * batch * base[i].k for grp in self.groups for i in grp[1:]
+            if self.x[i] is self.x[grp[0]])           # a shared x is read once
+        self.launches_per_layer = len(self.groups)
         self.cursor = 0
+
+    def run_layer(self, mats):
+        for grp in self.groups:
+            if len(grp) == 1:
+                i = grp[0]
+                self.lbt.gemv(mats[i], self.x[i], self.y[i])
+            else:
+                self.lbt.gemv_batched([(mats[i], self.x[i]) for i in grp], [self.y[i] for i in grp])
 
     def step(self):
         for _ in range(self.layers):
-            for i, pw in enumerate(self.sets[self.cursor % self.copies]):
-                self.lbt.gemv(pw, self.x[i], self.y[i])
+            self.run_layer(self.sets[self.cursor % self.copies])
             self.cursor += 1
 
     @property
@@ -215,26 +253,40 @@ def _want(name, sel):
     return sel is None or any(name.startswith(p) for p in sel)
 
 
+GEMV_ROWS = (  # row name, workload, batch, grouping
+    ("gemv_c1_b1", "c1", 1, "separate"),
+    ("gemv_c2_b1_7launches", "c2", 1, "separate"),
+    ("gemv_c2_b1_1launch", "c2", 1, "one"),
+    ("gemv_c3_b1", "c3", 1, "separate"),
+    ("gemv_c3_b4", "c3", 4, "separate"),
+    ("gemv_c4t_b1", "c4t", 1, "layer"),
+    ("gemv_c4t_b5", "c4t", 5, "layer"),
+    ("gemv_c4b_b1", "c4b", 1, "layer"),
+    ("gemv_c4b_b5", "c4b", 5, "layer"),
+    ("gemv_c4t_b1_5launches", "c4t", 1, "separate"),
+)
+
+
 def measure_gemv_rows(lbt, peaks, sel=None):
     rows = {}
-    for key, batches in (("c1", (1,)), ("c3", (1, 4)), ("c4t", (1, 5)), ("c4b", (1, 5))):
+    for name, key, b, grouping in GEMV_ROWS:
         wl = synth.WORKLOADS[key]
-        for b in batches:
-            if not _want(f"gemv_{key}_b{b}", sel):
-                continue
-            gs = GemvSet(wl, b, lbt)
-            steps = gs.copies * 2
-            g = _graph(lambda: [gs.step() for _ in range(steps)])
-            _time_graph(g)
-            ms = _time_graph(g, reps=3) / steps
-            gbs = gs.bytes_per_step / (ms * 1e-3) / 1e9
-            rows[f"gemv_{key}_b{b}"] = {
-                "shape": [[m.n, m.k] for m in wl.matrices], "fmt": wl.fmt, "x": wl.xdtype, "batch": b,
-                "us_per_layer_set": round(ms * 1e3, 3), "GB_s": round(gbs, 1),
-                "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 3),
-                "frac_of_8TBs_nominal": round(gbs / 8000.0, 3), "copies_rotated": gs.copies}
-            del gs, g
-            torch.cuda.empty_cache()
+        if not _want(name, sel):
+            continue
+        gs = GemvSet(wl, b, lbt, grouping=grouping)
+        steps = gs.copies * 2
+        g = _graph(lambda: [gs.step() for _ in range(steps)])
+        _time_graph(g)
+        ms = _time_graph(g, reps=3) / steps
+        gbs = gs.bytes_per_step / (ms * 1e-3) / 1e9
+        rows[name] = {
+            "shape": [[m.n, m.k] for m in wl.matrices], "fmt": wl.fmt, "x": wl.xdtype, "batch": b,
+            "launches": [[wl.matrices[i].name for i in grp] for grp in gs.groups],
+            "us_per_layer_set": round(ms * 1e3, 3), "GB_s": round(gbs, 1),
+            "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 3),
+            "frac_of_8TBs_nominal": round(gbs / 8000.0, 3), "copies_rotated": gs.copies}
+        del gs, g
+        torch.cuda.empty_cache()
     return rows
 
 
@@ -375,7 +427,9 @@ def run_reference(args, ws, rank):
 def _config():
     return {"workload": "c2: ternary g128 decode layer set of a 1.7B-class block (q,k,v,o 2048x2048; "
                         "gate,up 6144x2048; down 2048x6144), batch 1, x fp16, FP32 accumulate; "
-                        f"one step = one token through {LAYERS} distinct copies of the set",
+                        f"one step = one token through {LAYERS} distinct copies of the set, each issued as "
+                        "a decoder layer issues it: [q,k,v] on one x (one grouped launch), [o], [gate,up] on "
+                        "one x (one grouped launch), [down]",
             "global_batch": 1, "layers_per_step": LAYERS, "parallelism": "replicas",
             "l2": f"inputs larger than L2: {LAYERS} rotated copies (> 4x 126 MB) per step",
             "seeds": "synth.WORKLOADS['c2'].seed = 1002"}
@@ -387,7 +441,7 @@ def run_ours(args, ws, rank, local):
     torch.cuda.set_device(local)
     peaks = _peaks()
     wl = synth.WORKLOADS["c2"]
-    gs = GemvSet(wl, 1, lbt, copies=LAYERS, layers_per_step=LAYERS)
+    gs = GemvSet(wl, 1, lbt, copies=LAYERS, layers_per_step=LAYERS, grouping="layer")
     warm = _graph(lambda: [gs.step() for _ in range(max(1, args.warmup))])
     timed = _graph(lambda: [gs.step() for _ in range(args.steps)])
     launches = args.steps * LAYERS * gs.launches_per_layer
@@ -416,21 +470,21 @@ def run_ours(args, ws, rank, local):
     value = by_step * args.steps * ws / (ms_max * 1e-3) / 1e9
     per_rank_gbs = by_step * args.steps / (ms * 1e-3) / 1e9
 
-    # end to end through the public API with host buffers: per step the token's 7 activation
-    # vectors come from pinned host memory, all layers run eagerly through lb_gemv, and the 7
-    # outputs of the last layer are read back
-    xs_h = [x.cpu().pin_memory() for x in gs.x]
+    # end to end through the public API with host buffers: per step the token's activation
+    # vectors (one per launch group) come from pinned host memory, all layers run eagerly through
+    # lb_gemv / lb_gemv_batched, and the 7 outputs of the last layer are read back
+    heads = sorted({id(gs.x[i]): i for grp in gs.groups for i in grp}.values())   # distinct vectors
+    xs_h = {i: gs.x[i].cpu().pin_memory() for i in heads}
     ys_h = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in gs.y]
-    h2d = sum(x.numel() * x.element_size() for x in xs_h)
+    h2d = sum(x.numel() * x.element_size() for x in xs_h.values())
     d2h = sum(y.numel() * y.element_size() for y in ys_h)
     e2e_steps = max(3, min(args.steps, 20))
 
     def e2e_step():
-        for i in range(len(gs.x)):
+        for i in heads:
             gs.x[i].copy_(xs_h[i], non_blocking=True)
         for layer in range(LAYERS):
-            for i, pw in enumerate(gs.sets[layer % gs.copies]):
-                lbt.gemv(pw, gs.x[i], gs.y[i])
+            gs.run_layer(gs.sets[layer % gs.copies])
         for i in range(len(gs.y)):
             ys_h[i].copy_(gs.y[i], non_blocking=True)
         torch.cuda.current_stream().synchronize()
@@ -462,7 +516,8 @@ def run_ours(args, ws, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": _config(),
         "roofline": {"bound": "hbm", "achieved": round(per_rank_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(per_rank_gbs / peaks["hbm_gbs"], 4), "traffic": None,
-                     "kernel": "gemv_kernel<ternary, f16 x, batch 1> (7 launches per layer set)",
+                     "kernel": "gemv_kernel<ternary, f16 x, batch 1> (4 launches per layer set: "
+                               "q/k/v grouped, o, gate/up grouped, down)",
                      "achieved_basis": "algorithmic bytes (packed codes + scales + x + y) per launch / "
                                        "(timed region / launches), CUDA events, so launch gaps count against it",
                      "peak_basis": f"{peaks['source']} STREAM-style copy bandwidth"},
@@ -470,9 +525,9 @@ def run_ours(args, ws, rank, local):
                          "sample": f"the full layer set (7 matrices, 54.5 M weights), {cpu_passes} passes in "
                                    f"{cpu_dt:.1f} s, FP64 numpy oracle"},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "how": "per step: x of the 7 matrices copied from pinned host memory, LAYERS x 7 eager "
-                       "lb_gemv calls through the Python binding, the 7 outputs copied back, one stream "
-                       "synchronize; host wall clock"},
+                "how": "per step: the 4 activation vectors (one per launch group) copied from pinned host "
+                       "memory, LAYERS x 4 eager lb_gemv / lb_gemv_batched calls through the Python binding, "
+                       "the 7 outputs copied back, one stream synchronize; host wall clock"},
         "gpu_launches": launches,
         "clocks": clk,
         "peaks": peaks,
