@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   const uint32_t rank = a.S > 1 ? cluster_rank() : 0u;
   const int gpc = P.gpc;
   const int g_begin = static_cast<int>(rank) * gpc;
-  const int ng = min(gpc, P.G - g_begin);                        // groups of this CTA's chunk (>= 1)
+  const int ng = min(gpc, P.G - g_begin);                        // groups of this CTA's chunk (<= 0: none)
   const int nst = (ng + GS - 1) / GS;                            // stages per row block
   // row blocks of this CTA: rb0, rb0 + rb_stride, ... (grouped launch: exactly one)
   const int rb0 = static_cast<int>(blockIdx.y) - P.unit0;
@@ -583,6 +583,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     }
   }
 
+  if (a.S > 1 && ng <= 0) {
+    // a grouped launch splits every problem into S chunks; a short problem leaves some empty
+    float* red = reinterpret_cast<float*>(sm + L::red);
+    for (int i = threadIdx.x; i < ROWS * 8; i += kThreads) red[i] = 0.f;
+  }
   if (a.S > 1) {
     // one row block per cluster: the S K-chunks' partial sums meet in distributed shared memory;
     // every thread of every CTA (producer warp included) takes part in both cluster barriers
@@ -761,8 +766,10 @@ lb_status launch_t(const lb_weight& W, const uint16_t* x, int batch, uint16_t* y
                                    L::total(plan.gpc), st);
 }
 
-// Several GEMVs in one launch: one CTA per (problem, row block), whole K per CTA.  Problems with
-// the longest K get the first grid rows, so that the slowest CTAs start first.
+// Several GEMVs in one launch: one CTA (S > 1: one cluster of S CTAs, each a K chunk) per
+// (problem, row block).  One split S serves every problem (cluster dimensions are per launch); it
+// comes from the same time model as plan_split.  Problems with the longest K get the first grid
+// rows, so that the slowest CTAs start first.
 template <int FMT, bool XBF, int BP>
 lb_status launch_many(const lb_gemv_problem* probs, int count, int batch, cudaStream_t st) {
   using L = Layout<FMT, BP>;
@@ -774,25 +781,44 @@ lb_status launch_many(const lb_gemv_problem* probs, int count, int batch, cudaSt
       order[j] = order[j - 1];
       order[j - 1] = t;
     }
+  const int sms = lb::sm_count();
+  const double t_group = 16384.0 * (FmtTraits<FMT>::gbytes + 2) / 128.0 / 40.0;   // ns per 128x128 tile
+  int units = 0, gmax = 0;
+  for (int i = 0; i < count; ++i) {
+    units += static_cast<int>((probs[i].W.n + ROWS - 1) / ROWS);
+    gmax = max(gmax, static_cast<int>(probs[i].W.k / lb::kGroup));
+  }
+  auto chunk = [](int G, int S) { return S == 1 ? G : ((G + S - 1) / S + GS - 1) / GS * GS; };
+  int best_s = 0;
+  double best_t = 1e30;
+  for (int s_try = 1; s_try <= kMaxCluster; ++s_try) {
+    const int g = chunk(gmax, s_try);
+    if (s_try > 1 && (gmax + g - 1) / g != s_try) continue;        // the longest problem uses every rank
+    if (L::total(g) > kSmemMax) continue;
+    const int clusters = max(1, sms / s_try);
+    const int waves = (units + clusters - 1) / clusters;
+    const double t = waves * ((s_try == 1 ? 2500.0 : 3000.0) + g * t_group);
+    if (t < best_t * 0.999) { best_t = t; best_s = s_try; }
+  }
+  if (best_s == 0)
+    return lb::fail(LB_ERR_UNSUPPORTED, "lb_gemv_batched: K = %d too long at batch %d", gmax * lb::kGroup, batch);
   Args args;
   memset(&args, 0, sizeof(args));
-  int units = 0, smem = 0;
+  int smem = 0;
+  units = 0;
   for (int i = 0; i < count; ++i) {
     const lb_gemv_problem& pb = probs[order[i]];
-    const int G = static_cast<int>(pb.W.k / lb::kGroup);
-    if (L::total(G) > kSmemMax)
-      return lb::fail(LB_ERR_UNSUPPORTED, "lb_gemv_batched: K = %lld too long for one CTA at batch %d",
-                      static_cast<long long>(pb.W.k), batch);
-    lb_status s = fill_prob<FMT>(pb.W, pb.x, pb.y, G, args.p[i]);
+    const int gpc = chunk(static_cast<int>(pb.W.k / lb::kGroup), best_s);
+    lb_status s = fill_prob<FMT>(pb.W, pb.x, pb.y, gpc, args.p[i]);
     if (s != LB_OK) return s;
     args.p[i].unit0 = units;
     units += args.p[i].row_blocks;
-    smem = max(smem, L::total(G));
+    smem = max(smem, L::total(gpc));
   }
   args.count = count;
   args.batch = batch;
-  args.S = 1;
-  return launch_args<FMT, XBF, BP>(args, 1, units, smem, st);
+  args.S = best_s;
+  return launch_args<FMT, XBF, BP>(args, best_s, units, smem, st);
 }
 
 template <int FMT, bool XBF>

@@ -130,7 +130,9 @@ lb_status lb_pack_ternary(const int8_t* t, const uint16_t* s_in, int64_t n, int6
  * x     : device [batch][k] of `xdt`, 16-byte aligned.     y : device [batch][n] of `xdt`.
  * batch : 1 .. 8.
  * Asynchronous on `stream`.  Errors (no launch): LB_ERR_NULL, LB_ERR_SHAPE, LB_ERR_ALIGN,
- * LB_ERR_DTYPE; LB_ERR_CUDA if the launch fails.
+ * LB_ERR_DTYPE; LB_ERR_UNSUPPORTED if k is longer than 8 CTAs of a cluster hold in shared memory
+ * (k <= 352256 at batch 1, 196608 at batch 2, 98304 at batch 3-4, 49152 at batch 5-8);
+ * LB_ERR_CUDA if the launch fails.
  */
 lb_status lb_gemv(const lb_weight* W, const void* x, int xdt, int batch, void* y, lb_stream stream);
 
@@ -154,8 +156,7 @@ typedef struct lb_gemv_problem {
  * xdt      : LB_F16 or LB_BF16 for every x and y;  batch : 1 .. 8 for every problem.
  * No y may overlap another problem's x or y.  Asynchronous on `stream`.  Errors (no launch):
  * LB_ERR_NULL, LB_ERR_SHAPE (count or batch out of range, a bad n / k), LB_ERR_ALIGN, LB_ERR_DTYPE,
- * LB_ERR_UNSUPPORTED (mixed formats, or a k too long for one CTA: k <= 44672 at batch 1, 24832 at
- * batch 2, 13056 at batch 3-4, 6784 at batch 5-8), LB_ERR_CUDA if the launch fails.
+ * LB_ERR_UNSUPPORTED (mixed formats, or a k above the lb_gemv limit), LB_ERR_CUDA if the launch fails.
  */
 lb_status lb_gemv_batched(const lb_gemv_problem* problems, int count, int xdt, int batch, lb_stream stream);
 

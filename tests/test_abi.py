@@ -111,7 +111,8 @@ def test_gemv_batched_validation():
     assert _status(lb.lb_gemv_batched, [ok, (W1, None, A16)], lb.LB_F16, 1) == "LB_ERR_NULL"
     assert _status(lb.lb_gemv_batched, [ok, (W1, A16, MIS)], lb.LB_F16, 1) == "LB_ERR_ALIGN"
     assert _status(lb.lb_gemv_batched, [ok, (lb.make_weight(1, 16, 130, A16, A16), A16, A16)], lb.LB_F16, 1) == "LB_ERR_SHAPE"
-    # one CTA holds the whole K of a problem: the documented limits
-    for batch, kmax in ((1, 44672), (2, 24832), (4, 13056), (8, 6784)):
+    # the documented k limits (an 8-CTA split), for the grouped and the single call
+    for batch, kmax in ((1, 352256), (2, 196608), (4, 98304), (8, 49152)):
         long_w = lb.make_weight(lb.LB_FMT_1BIT_G128, 16, kmax + 128, A16, A16)
         assert _status(lb.lb_gemv_batched, [(long_w, A16, A16)], lb.LB_F16, batch) == "LB_ERR_UNSUPPORTED"
+        assert _status(lb.lb_gemv, long_w, A16, lb.LB_F16, batch, A16, 0) == "LB_ERR_UNSUPPORTED"

@@ -171,3 +171,18 @@ def test_gemv_batched_c2_layer_set_grouping():
             scales = u16(pw.scales).reshape(mat.n, -1)
             y_ref, a = oracle_products("ternary", codes, scales, mat.k, x.cpu())
             check_products(y, y_ref, a, f"c2/{name} grouped")
+
+
+@pytest.mark.parametrize("fmt", ["1bit", "ternary"])
+@pytest.mark.parametrize("batch", [1, 5])
+def test_gemv_batched_k_split_with_empty_chunks(fmt, batch):
+    """A long-K problem with few rows makes the grouped launch split K over a cluster; the short
+    problems of the same launch then have K chunks with no groups, which must add nothing."""
+    shapes = [(64, 8192), (16, 256), (200, 1024), (130, 128)]
+    packed = [_packed(fmt, n, k, seed=2 * n + k) for n, k in shapes]
+    xs = [synth.activations(batch, k, "bf16", seed=n + k).cuda() for n, k in shapes]
+    ys = tensors.gemv_batched([(pw, x) for (pw, _, _), x in zip(packed, xs)])
+    torch.cuda.synchronize()
+    for (pw, codes, scales), (n, k), x, y in zip(packed, shapes, xs, ys):
+        y_ref, a = oracle_products(fmt, codes, scales, k, x.cpu())
+        check_products(y, y_ref, a, f"batched split {fmt} n={n} k={k} batch={batch}")
