@@ -44,6 +44,10 @@ if ROOT not in sys.path:
 from gemm_lb_gemv_02_b300 import synth  # noqa: E402
 
 LAYERS = 36                      # distinct layer-set copies per step (weights >> L2)
+# DRAM bytes per headline GEMV launch from an ncu capture of one layer set (14.62 MB / 4 launches);
+# the algorithmic bytes are 14.55 MB per set, so nothing is re-read.  Set to None when the kernel
+# changes until a new capture is taken.
+GEMV_TRAFFIC_PER_LAUNCH = 3.656e6
 L2_BYTES = 126 * 2 ** 20
 METRIC = "packed-weight GEMV HBM GB/s (% of peak) at batch 1; prefill GEMM TFLOP/s"
 
@@ -515,7 +519,10 @@ def run_ours(args, ws, rank, local):
         "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": _config(),
         "roofline": {"bound": "hbm", "achieved": round(per_rank_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(per_rank_gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                     "frac": round(per_rank_gbs / peaks["hbm_gbs"], 4), "traffic": GEMV_TRAFFIC_PER_LAUNCH,
+                     "traffic_basis": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one layer set "
+                                      "(4 launches) / 4, bytes per launch; kernel as of commit c0af558 "
+                                      "(summary under profiles/, gemv_kernel on the c2 layer set)",
                      "kernel": "gemv_kernel<ternary, f16 x, batch 1> (4 launches per layer set: "
                                "q/k/v grouped, o, gate/up grouped, down)",
                      "achieved_basis": "algorithmic bytes (packed codes + scales + x + y) per launch / "
