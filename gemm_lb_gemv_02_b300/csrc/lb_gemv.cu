@@ -664,13 +664,24 @@ Plan plan_split(int G, int row_blocks, int sms) {
   return best;
 }
 
-// Tensor maps and sizes of one problem (gpc: groups per K chunk of the launch's split).
+// Tensor maps of a weight depend only on its planes' addresses, its shape and its format, so they
+// are encoded once and kept in a small direct-mapped host cache (a hit is checked field by field;
+// a miss re-encodes and replaces the entry).
+struct MapEntry {
+  const uint8_t* codes;
+  const uint16_t* scales;
+  int64_t n, k;
+  int fmt, valid;
+  CUtensorMap tm_codes, tm_scales;
+};
+constexpr int kMapCache = 1024;
+MapEntry g_maps[kMapCache];
+std::mutex g_maps_mu;
+
 template <int FMT>
-lb_status fill_prob(const lb_weight& W, const void* x, void* y, int gpc, Prob& pr) {
+lb_status encode_maps(const lb_weight& W, CUtensorMap& tm_codes, CUtensorMap& tm_scales, int scales_tma) {
   const int n = static_cast<int>(W.n), k = static_cast<int>(W.k), G = k / lb::kGroup;
   const int gbytes = FmtTraits<FMT>::gbytes;
-  memset(&pr, 0, sizeof(pr));
-  pr.scales_tma = (G % 8 == 0) ? 1 : 0;                            // scales row stride: 16-byte multiple
   EncodeTiledFn enc = encode_fn();
   if (!enc) return lb::fail(LB_ERR_CUDA, "lb_gemv: cuTensorMapEncodeTiled unavailable");
   {
@@ -678,20 +689,47 @@ lb_status fill_prob(const lb_weight& W, const void* x, void* y, int gpc, Prob& p
     const cuuint64_t strides[1] = {dims[0]};
     const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(ROWS)};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(&pr.tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(W.codes), dims, strides,
+    CUresult r = enc(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(W.codes), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return lb::fail(LB_ERR_CUDA, "lb_gemv: codes tensor map (CUresult %d)", static_cast<int>(r));
   }
-  if (pr.scales_tma) {
+  if (scales_tma) {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(G), static_cast<cuuint64_t>(n)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(G) * 2};
     const cuuint32_t box[2] = {8, static_cast<cuuint32_t>(ROWS)};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(&pr.tm_scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t*>(W.scales), dims,
+    CUresult r = enc(&tm_scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t*>(W.scales), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return lb::fail(LB_ERR_CUDA, "lb_gemv: scales tensor map (CUresult %d)", static_cast<int>(r));
+  }
+  return LB_OK;
+}
+
+// Tensor maps and sizes of one problem (gpc: groups per K chunk of the launch's split).
+template <int FMT>
+lb_status fill_prob(const lb_weight& W, const void* x, void* y, int gpc, Prob& pr) {
+  const int n = static_cast<int>(W.n), k = static_cast<int>(W.k), G = k / lb::kGroup;
+  memset(&pr, 0, sizeof(pr));
+  pr.scales_tma = (G % 8 == 0) ? 1 : 0;                            // scales row stride: 16-byte multiple
+  {
+    const uintptr_t h = (reinterpret_cast<uintptr_t>(W.codes) >> 8) ^ (reinterpret_cast<uintptr_t>(W.codes) >> 20);
+    std::lock_guard<std::mutex> lk(g_maps_mu);
+    MapEntry& e = g_maps[h % kMapCache];
+    if (!(e.valid && e.codes == W.codes && e.scales == W.scales && e.n == W.n && e.k == W.k && e.fmt == W.fmt)) {
+      e.valid = 0;
+      lb_status s = encode_maps<FMT>(W, e.tm_codes, e.tm_scales, pr.scales_tma);
+      if (s != LB_OK) return s;
+      e.codes = W.codes;
+      e.scales = W.scales;
+      e.n = W.n;
+      e.k = W.k;
+      e.fmt = W.fmt;
+      e.valid = 1;
+    }
+    pr.tm_codes = e.tm_codes;
+    pr.tm_scales = e.tm_scales;
   }
   pr.scales = W.scales;
   pr.x = static_cast<const uint16_t*>(x);

@@ -95,10 +95,23 @@ def _ptr(obj) -> int | None:
     return int(obj)
 
 
+_torch = None
+_have_cuda = None
+
+
 def _stream(stream) -> int | None:
+    global _torch, _have_cuda
     if stream is None:
-        import torch
-        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+        if _have_cuda is None:
+            import torch
+            _torch = torch
+            _have_cuda = torch.cuda.is_available()
+            if _have_cuda:
+                torch.cuda.init()
+        if not _have_cuda:
+            return None
+        # torch's current stream on the current device, as a raw cudaStream_t
+        return _torch._C._cuda_getCurrentRawStream(_torch._C._cuda_getDevice())
     if hasattr(stream, "cuda_stream"):
         return stream.cuda_stream
     return int(stream)

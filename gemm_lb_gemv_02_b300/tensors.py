@@ -6,7 +6,7 @@ method happens here.
 
 from __future__ import annotations
 
-from dataclasses import dataclass
+from dataclasses import dataclass, field
 
 import torch
 
@@ -31,9 +31,14 @@ class PackedWeight:
     k: int
     codes: torch.Tensor
     scales: torch.Tensor
+    _struct: object = field(default=None, repr=False, compare=False)
 
     def struct(self) -> lb.lb_weight:
-        return lb.make_weight(self.fmt, self.n, self.k, self.codes, self.scales)
+        """The C lb_weight of this matrix (rebuilt only when a plane was replaced)."""
+        key = (self.fmt, self.n, self.k, self.codes.data_ptr(), self.scales.data_ptr())
+        if self._struct is None or self._struct[0] != key:
+            self._struct = (key, lb.make_weight(self.fmt, self.n, self.k, self.codes, self.scales))
+        return self._struct[1]
 
     @classmethod
     def empty(cls, fmt: int, n: int, k: int, device="cuda") -> "PackedWeight":
