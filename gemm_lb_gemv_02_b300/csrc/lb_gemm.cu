@@ -9,31 +9,41 @@
 // every product is exact in the FP32 accumulator, so the group scale costs nothing inside the
 // k-loop.  BF16 activations are converted to binary16 once (exact for normal-range values).
 //
-// Structure (one 128 x 256 output tile per CTA, K in steps of 64):
+// Structure (one tile of 128 weight rows x 256 tokens per CTA, K in steps of 64): the decoded
+// weights are the MMA's A operand and live in tensor memory; the activations are the B operand in
+// shared memory.  Decoder threads own weight rows, i.e. TMEM lanes, so their decoded registers go to
+// TMEM with tcgen05.st and never pass through shared memory, which then carries only the
+// activation tiles (one bulk-copy write and one tensor-core read per byte).
 //   * prologue kernel: X -> binary16, K permuted inside each 16-block to match the decoder's
-//     register order, written as ready-made 128-byte-swizzled shared-memory images of the
-//     128 x 64 A tiles (one 16 KB contiguous block per tile), so that one bulk copy moves a tile;
-//   * warp 8 (one lane): bulk-copies A tiles into a STAGES-deep ring (mbarrier complete_tx);
-//   * warps 0-7: thread i owns weight row n0 + i, loads its 2-bit codes and scale, decodes them
-//     with one LOP3 + two half2 ops per two weights into the swizzled B tile, and arrives;
-//   * warp 9: allocates TMEM (256 columns), one lane issues tcgen05.mma kind::f16 (M128 N256 K16)
-//     and commits each stage back to the producers;
-//   * epilogue: warps 0-7 read the FP32 accumulator with tcgen05.ld and store BF16/FP16 rows.
-// Every mbarrier wait is bounded; a timeout sets a bit in the device error word and the CTA
-// finishes (TMEM is always released).
+//     register order, written as ready-made 128-byte-swizzled shared-memory images of 128-token
+//     x 64 tiles (one 16 KB contiguous block per tile), so that one bulk copy moves a tile;
+//   * warp 8 (one lane): after griddepcontrol.wait, bulk-copies two such tiles (256 tokens) per
+//     stage into a STAGES-deep ring (mbarrier complete_tx);
+//   * warps 0-7: warp w owns TMEM lanes 32(w % 4) .. +31 (weight rows n0 + lane) and half of each
+//     stage's K; it loads 2-bit codes and the group scale, decodes them with one LOP3 + two half2
+//     ops per two weights and stores the stage's A columns with tcgen05.st;
+//   * warp 9: allocates TMEM (4 A stages x 32 columns + a 256-column FP32 accumulator), one lane
+//     issues tcgen05.mma kind::f16 (M128 N256 K16, A from TMEM) and commits each stage back;
+//   * epilogue: warps 0-7 read the accumulator with tcgen05.ld (lane = weight row, column =
+//     token) and store BF16/FP16 Y[token][row].
+// The GEMM is launched with programmatic dependent launch, so the weight decode of the first
+// stages overlaps the activation prologue.  Every mbarrier wait is bounded; a timeout sets a bit in
+// the device error word and the CTA finishes (TMEM is always released).
 #include <mutex>
 
 #include "lb_common.cuh"
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;   // 16 KB
-constexpr int B_BYTES = BN * BK * 2;   // 32 KB
+constexpr int BM = 128, BK = 64, STAGES = 4;     // BM: tokens per activation tile
+constexpr int WM = 128, TN = 256;                 // weight rows and tokens per CTA (MMA M and N)
+constexpr int A_BYTES = BM * BK * 2;              // one activation tile: 16 KB
+constexpr int X_BYTES = 2 * A_BYTES;              // activation stage: 256 tokens x 64
 constexpr int kDecodeWarps = 8;
 constexpr int kThreads = (kDecodeWarps + 2) * 32;
-constexpr uint32_t kTmemCols = 256;
-constexpr size_t kSmemBytes = 1024 + STAGES * (A_BYTES + B_BYTES) + 256;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAcc = 256;                    // first accumulator column
+constexpr size_t kSmemBytes = 1024 + STAGES * X_BYTES + 256;
 
 // ------------------------------------------------------------------------------- prologue
 // One thread per (row, 16-wide K block): 16 activations -> binary16, positions 2p / 2p+1 of the
@@ -42,6 +52,7 @@ template <bool BF>
 __global__ void __launch_bounds__(256) xprep_kernel(const uint16_t* __restrict__ x, int64_t m, int k,
                                                     int64_t total, uint8_t* __restrict__ ws,
                                                     uint32_t* __restrict__ err) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // the GEMM may start decoding weights
   const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (gid >= total) return;
   const int kb = k / 16;
@@ -117,31 +128,51 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 }
 
 // ------------------------------------------------------------------------------- main kernel
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// 32 lanes x 16 consecutive columns; thread i writes lane (base lane + i), register j -> column j.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_ternary_kernel(const uint8_t* __restrict__ ws_a, const uint8_t* __restrict__ codes,
-                        const uint16_t* __restrict__ scales, uint16_t* __restrict__ y, int m, int n, int k,
-                        int y_bf16, uint32_t* __restrict__ err) {
+    gemm_ternary_kernel(const uint8_t* __restrict__ ws_x, const uint8_t* __restrict__ codes,
+                        const uint16_t* __restrict__ scales, uint16_t* __restrict__ y, int m, int mpad, int n,
+                        int k, int y_bf16, uint32_t* __restrict__ err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + STAGES * A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
-  uint64_t* full_a = bars;
-  uint64_t* full_b = bars + STAGES;
+  uint8_t* sX = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sX + STAGES * X_BYTES);
+  uint64_t* full_x = bars;
+  uint64_t* a_full = bars + STAGES;
   uint64_t* empty = bars + 2 * STAGES;
   uint64_t* tmem_full = bars + 3 * STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * BN;
-  const int mt = blockIdx.y;
-  const int m0 = mt * BM;
+  const int n0 = blockIdx.x * WM;
+  const int t0 = blockIdx.y * TN;                                  // first token of the tile
+  const int ntiles = min(2, (mpad - t0) / BM);                     // 128-token activation tiles (1 or 2)
   const int KT = k / BK;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      lbdev::mbar_init(&full_a[s], 1);
-      lbdev::mbar_init(&full_b[s], kDecodeWarps * 32);
+      lbdev::mbar_init(&full_x[s], 1);
+      lbdev::mbar_init(&a_full[s], kDecodeWarps);
       lbdev::mbar_init(&empty[s], 1);
     }
     lbdev::mbar_init(tmem_full, 1);
@@ -158,101 +189,94 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool ok = true;
 
   if (warp == kDecodeWarps) {
-    // ---------------- A producer
+    // ---------------- activation producer (the prologue kernel wrote the tiles)
+    griddep_wait();
     if (lane == 0) {
+      const uint32_t bytes = static_cast<uint32_t>(ntiles * A_BYTES);
+      const size_t mt0 = static_cast<size_t>(t0 / BM);
       for (int it = 0; it < KT; ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
         if (!lbdev::mbar_wait(&empty[s], ph ^ 1)) { ok = false; break; }
-        lbdev::mbar_arrive_expect_tx(&full_a[s], A_BYTES);
-        lbdev::bulk_g2s(sA + s * A_BYTES, ws_a + (static_cast<size_t>(mt) * KT + it) * A_BYTES, A_BYTES, &full_a[s]);
+        lbdev::mbar_arrive_expect_tx(&full_x[s], bytes);
+        for (int tt = 0; tt < ntiles; ++tt)
+          lbdev::bulk_g2s(sX + s * X_BYTES + tt * A_BYTES, ws_x + ((mt0 + tt) * KT + it) * A_BYTES, A_BYTES,
+                          &full_x[s]);
       }
     }
   } else if (warp == kDecodeWarps + 1) {
     // ---------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = lbdev::idesc_f16_f32(BM, BN);
+      const uint32_t idesc = lbdev::idesc_f16_f32(WM, static_cast<uint32_t>(ntiles * BM));
       for (int it = 0; it < KT; ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1;
-        if (!lbdev::mbar_wait(&full_a[s], ph) || !lbdev::mbar_wait(&full_b[s], ph)) { ok = false; break; }
+        if (!lbdev::mbar_wait(&full_x[s], ph) || !lbdev::mbar_wait(&a_full[s], ph)) { ok = false; break; }
         lbdev::tc_fence_after();
-        const uint32_t a_base = lbdev::smem_u32(sA + s * A_BYTES);
-        const uint32_t b_base = lbdev::smem_u32(sB + s * B_BYTES);
+        const uint32_t x_base = lbdev::smem_u32(sX + s * X_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          lbdev::tc_mma_f16(tmem, lbdev::smem_desc_sw128(a_base + 32 * kk), lbdev::smem_desc_sw128(b_base + 32 * kk),
-                            idesc, (it | kk) != 0 ? 1u : 0u);
-        }
-        lbdev::tc_commit(&empty[s]);
+        for (int kk = 0; kk < BK / 16; ++kk)
+          tc_mma_f16_ts(tmem + kAcc, tmem + static_cast<uint32_t>(32 * s + 8 * kk),
+                        lbdev::smem_desc_sw128(x_base + 32 * kk), idesc, (it | kk) != 0 ? 1u : 0u);
+        lbdev::tc_commit(&empty[s]);                               // frees the A columns and the X slot
       }
       lbdev::tc_commit(tmem_full);
     }
   } else {
-    // ---------------- B decoders: thread i <-> weight row n0 + i
-    const int i = threadIdx.x;
-    const int row = n0 + i;
-    const bool valid = row < n;
+    // ---------------- weight decoders: warp w -> TMEM lanes 32q.. (rows n0 + 32q + lane), K half h
+    const int q = warp & 3, h = warp >> 2;
+    const int row = 32 * q + lane;
+    const int wrow = n0 + row;
+    const bool valid = wrow < n;
     const int G = k / lb::kGroup;
-    const uint4* crow = reinterpret_cast<const uint4*>(codes + static_cast<int64_t>(valid ? row : 0) * (k / 4));
-    const uint16_t* srow = scales + static_cast<int64_t>(valid ? row : 0) * G;
-    const uint32_t sw = static_cast<uint32_t>(i & 7);
-    uint4 nc0 = make_uint4(0, 0, 0, 0), nc1 = nc0;
+    const uint8_t* crow = codes + static_cast<int64_t>(valid ? wrow : 0) * (k / 4) + 8 * h;
+    const uint16_t* srow = scales + static_cast<int64_t>(valid ? wrow : 0) * G;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
+    uint2 nc = make_uint2(0u, 0u);
     uint32_t ns = 0;
-    if (valid) { nc0 = __ldg(crow); nc1 = __ldg(crow + 1); ns = __ldg(srow); }
-    for (int g = 0; g < G && ok; ++g) {
-      const uint4 c0 = nc0, c1 = nc1;
+    if (valid) { nc = __ldg(reinterpret_cast<const uint2*>(crow)); ns = __ldg(srow); }
+    for (int it = 0; it < KT && ok; ++it) {
+      const int s = it % STAGES;
+      const uint32_t ph = (it / STAGES) & 1;
+      const uint2 c = nc;
       const uint32_t s2 = ns * 0x00010001u;
-      if (valid && g + 1 < G) { nc0 = __ldg(crow + 2 * (g + 1)); nc1 = __ldg(crow + 2 * (g + 1) + 1); ns = __ldg(srow + g + 1); }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int it = 2 * g + h;
-        const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1;
-        if (!lbdev::mbar_wait(&empty[s], ph ^ 1)) { ok = false; break; }
-        const uint4 c = h ? c1 : c0;
-        const uint32_t words[4] = {c.x, c.y, c.z, c.w};
-        const uint32_t dst = lbdev::smem_u32(sB + s * B_BYTES + i * 128);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          uint32_t o[8];
-          decode_word_st(words[u], s2, o);
-          st_shared_v4(dst + (((2u * u) ^ sw) << 4), o[0], o[1], o[2], o[3]);
-          st_shared_v4(dst + (((2u * u + 1u) ^ sw) << 4), o[4], o[5], o[6], o[7]);
-        }
-        lbdev::fence_proxy_async_smem();
-        lbdev::mbar_arrive(&full_b[s]);
+      if (valid && it + 1 < KT) {                                  // next stage: 16 bytes of codes per row
+        nc = __ldg(reinterpret_cast<const uint2*>(crow + 16 * (it + 1)));
+        ns = __ldg(srow + (it + 1) / 2);
       }
+      uint32_t o[16];
+      {
+        uint32_t a8[8], b8[8];
+        decode_word_st(c.x, s2, a8);
+        decode_word_st(c.y, s2, b8);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { o[i] = a8[i]; o[8 + i] = b8[i]; }
+      }
+      if (!lbdev::mbar_wait(&empty[s], ph ^ 1)) { ok = false; break; }   // the stage's MMAs retired
+      lbdev::tc_fence_after();
+      tmem_st16(lane_base + static_cast<uint32_t>(32 * s + 16 * h), o);
+      tmem_st_wait();
+      lbdev::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) lbdev::mbar_arrive(&a_full[s]);
     }
-    // ---------------- epilogue
+    // ---------------- epilogue: lane = weight row, columns = tokens
     if (!lbdev::mbar_wait(tmem_full, 0)) ok = false;
     lbdev::tc_fence_after();
-    const int quad = warp & 3, half = warp >> 2;
-    const int token = m0 + 32 * quad + lane;
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
-      const int col = 128 * half + 32 * c;
+      const int col = 128 * h + 32 * c;                            // token offset in the tile
       uint32_t v[32];
-      lbdev::tmem_ld32(tmem + (static_cast<uint32_t>(32 * quad) << 16) + static_cast<uint32_t>(col), v);
+      lbdev::tmem_ld32(lane_base + kAcc + static_cast<uint32_t>(col), v);
       lbdev::tmem_ld_wait();
-      if (token < m) {
-        uint16_t* dst = y + static_cast<int64_t>(token) * n + n0 + col;
+      if (valid) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (n0 + col + 8 * j + 8 <= n) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float a = __uint_as_float(v[8 * j + 2 * e]), b = __uint_as_float(v[8 * j + 2 * e + 1]);
-              if (y_bf16) {
-                const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-                pk[e] = *reinterpret_cast<const uint32_t*>(&h);
-              } else {
-                const __half2 h = __floats2half2_rn(a, b);
-                pk[e] = *reinterpret_cast<const uint32_t*>(&h);
-              }
-            }
-            *reinterpret_cast<uint4*>(dst + 8 * j) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        for (int j = 0; j < 32; ++j) {
+          const int tok = t0 + col + j;
+          if (tok < m) {
+            const float f = __uint_as_float(v[j]);
+            y[static_cast<int64_t>(tok) * n + wrow] =
+                y_bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(f)) : __half_as_ushort(__float2half_rn(f));
           }
         }
       }
@@ -345,11 +369,19 @@ lb_status launch_gemm(const lb_weight& W, const void* x, int xdt, int64_t m, voi
       if (dev >= 0 && dev < 64) done[dev] = true;
     }
   }
-  const dim3 grid((n + BN - 1) / BN, static_cast<unsigned>(mpad / BM));
-  gemm_ternary_kernel<<<grid, kThreads, kSmemBytes, st>>>(static_cast<const uint8_t*>(ws), W.codes, W.scales,
-                                                          static_cast<uint16_t*>(y), static_cast<int>(m), n, k,
-                                                          ydt == LB_BF16 ? 1 : 0, err);
-  e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((n + WM - 1) / WM, static_cast<unsigned>((mpad + TN - 1) / TN), 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // overlap the prologue kernel
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, gemm_ternary_kernel, static_cast<const uint8_t*>(ws), W.codes, W.scales,
+                         static_cast<uint16_t*>(y), static_cast<int>(m), static_cast<int>(mpad), n, k,
+                         ydt == LB_BF16 ? 1 : 0, err);
   if (e != cudaSuccess) return cuda_fail(e, "lb_gemm: launch");
   return LB_OK;
 }
