@@ -335,30 +335,48 @@ def measure_pack_rows(lbt, peaks, sel=None):
     return rows
 
 
-def measure_gemm_row(lbt, peaks, sel=None):
-    if not _want("gemm_c5", sel):
-        return {}
-    wl = synth.WORKLOADS["c5"]
-    base = _pack_workload(wl, lbt)[0]
-    x = synth.workload_activations(wl, 0, 512).cuda()
-    per_copy = _gemv_bytes(base, 0) + x.numel() * 2 + 512 * base.n * 2
+GEMM_ROWS = (
+    # name, workload, matrix index, tokens
+    ("gemm_c5", "c5", 0, 512),
+    ("gemm_c4b_1bit_gate", "c4b", 2, 512),
+    ("gemm_c5_m16", "c5", 0, 16),
+    ("gemm_c5_m64", "c5", 0, 64),
+    ("gemm_c5_m128", "c5", 0, 128),
+)
+
+
+def _gemm_one(lbt, peaks, wl_key, index, m):
+    wl = synth.WORKLOADS[wl_key]
+    base = _pack_workload(wl, lbt)[index]
+    x = synth.workload_activations(wl, index, m).cuda()
+    wbytes = _gemv_bytes(base, 0)
+    per_copy = wbytes + x.numel() * 2 + m * base.n * 2
     copies = _copies_for(per_copy)
     ws = [base] + [_clone(base) for _ in range(copies - 1)]
     xs = [x.clone() for _ in range(copies)]
-    y = torch.empty(512, base.n, dtype=torch.bfloat16, device="cuda")
-    wsp = torch.empty(lbt.lb.lb_gemm_workspace_bytes(512, base.n, base.k, lbt.lb.LB_BF16), dtype=torch.uint8,
+    y = torch.empty(m, base.n, dtype=torch.bfloat16, device="cuda")
+    wsp = torch.empty(lbt.lb.lb_gemm_workspace_bytes(m, base.n, base.k, lbt.lb.LB_BF16), dtype=torch.uint8,
                       device="cuda")
     steps = copies * 2
     g = _graph(lambda: [lbt.gemm(ws[i % copies], xs[i % copies], torch.bfloat16, y, wsp) for i in range(steps)])
     _time_graph(g)
     ms = _time_graph(g, reps=3) / steps
-    flops = 2.0 * 512 * base.n * base.k
+    flops = 2.0 * m * base.n * base.k
     tf = flops / (ms * 1e-3) / 1e12
-    return {"gemm_c5": {"shape": [512, base.k, base.n], "us_per_gemm": round(ms * 1e3, 2),
-                        "TFLOP_s": round(tf, 1), "frac_of_measured_bf16_burst": round(tf / peaks["bf16_tflops"], 3),
-                        "frac_of_measured_bf16_sustained": round(tf / peaks["bf16_tflops_sustained"], 3)
-                        if peaks.get("bf16_tflops_sustained") else None,
-                        "includes": "activation conversion prologue + GEMM kernel", "copies_rotated": copies}}
+    return {"format": wl.fmt, "shape": [m, base.k, base.n], "us_per_gemm": round(ms * 1e3, 2),
+            "TFLOP_s": round(tf, 1), "frac_of_measured_bf16_burst": round(tf / peaks["bf16_tflops"], 3),
+            "frac_of_measured_bf16_sustained": round(tf / peaks["bf16_tflops_sustained"], 3)
+            if peaks.get("bf16_tflops_sustained") else None,
+            "weight_GB_s": round(wbytes / (ms * 1e-3) / 1e9, 1),
+            "includes": "activation conversion prologue + GEMM kernel", "copies_rotated": copies}
+
+
+def measure_gemm_row(lbt, peaks, sel=None):
+    rows = {}
+    for name, wl_key, index, m in GEMM_ROWS:
+        if _want(name, sel):
+            rows[name] = _gemm_one(lbt, peaks, wl_key, index, m)
+    return rows
 
 
 def cpu_baseline(seconds: float = 10.0):

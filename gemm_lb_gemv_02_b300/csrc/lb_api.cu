@@ -197,7 +197,6 @@ lb_status lb_gemm(const lb_weight* W, const void* x, int xdt, int64_t m, void* y
   if (!valid_dtype(xdt) || !valid_dtype(ydt)) return fail(LB_ERR_DTYPE, "unknown dtype (x %d, y %d)", xdt, ydt);
   if (m < 1 || m > (int64_t(1) << 24)) return fail(LB_ERR_SHAPE, "m must be in [1, 2^24] (got %lld)", (long long)m);
   if (W->n % 16) return fail(LB_ERR_SHAPE, "lb_gemm needs n %% 16 == 0 (got %lld)", (long long)W->n);
-  if (W->fmt != LB_FMT_TERNARY_G128) return fail(LB_ERR_UNSUPPORTED, "lb_gemm implements the ternary format only");
   if (!lb::aligned16(x) || !lb::aligned16(y)) return fail(LB_ERR_ALIGN, "x and y must be 16-byte aligned");
   const size_t need = lb::gemm_workspace_bytes(m, W->k);
   if (need && (!workspace || workspace_bytes < need))
@@ -215,8 +214,6 @@ lb_status lb_gemm_noalloc(const lb_weight* W, const void* x, int xdt, int64_t m,
   if (!valid_dtype(xdt) || !valid_dtype(ydt)) return fail(LB_ERR_DTYPE, "unknown dtype (x %d, y %d)", xdt, ydt);
   if (m < 1 || m > (int64_t(1) << 24)) return fail(LB_ERR_SHAPE, "m must be in [1, 2^24] (got %lld)", (long long)m);
   if (W->n % 16) return fail(LB_ERR_SHAPE, "lb_gemm_noalloc needs n %% 16 == 0 (got %lld)", (long long)W->n);
-  if (W->fmt != LB_FMT_TERNARY_G128)
-    return fail(LB_ERR_UNSUPPORTED, "lb_gemm_noalloc implements the ternary format only");
   if (!lb::aligned16(x) || !lb::aligned16(y)) return fail(LB_ERR_ALIGN, "x and y must be 16-byte aligned");
   return lb::launch_gemm_noalloc(*W, x, xdt, m, y, ydt, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -2,6 +2,7 @@
 // sm_103a features the kernels use (mbarrier, bulk async copies, tcgen05 / TMEM).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
@@ -19,6 +20,13 @@ lb_status fail(lb_status s, const char* fmt, ...);           // records the thre
 lb_status cuda_fail(cudaError_t e, const char* where);       // LB_ERR_CUDA with the CUDA text
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 int sm_count();                                              // SMs of the current device
+
+// cuTensorMapEncodeTiled, looked up once through the runtime's driver entry point (nullptr if the
+// driver does not provide it).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tensor_map_encoder();
 
 // Device word with sticky error bits (see lb_device_error); one per device, owned by lb_api.cu.
 uint32_t* device_error_word();
@@ -78,12 +86,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait: returns false (and the caller reports an error) if the phase does not flip within
-// roughly `limit` polls.  Each try_wait may suspend the thread for a short hardware-defined time.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit = (1u << 24)) {
-  for (uint32_t i = 0; i < limit; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-  }
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait: returns false (and the caller reports an error) if the phase has not completed
+// after about `limit_ns` nanoseconds of global time.  Each try_wait carries a suspend-time hint, so
+// a waiting thread sleeps in the barrier unit until the phase completes instead of spinning and
+// taking issue slots from the threads that do the work.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  do {
+    if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
+  } while (globaltimer_ns() - t0 < limit_ns);
   return false;
 }
 

@@ -182,7 +182,7 @@ __device__ __forceinline__ float4 lds128f(uint32_t a) {
 constexpr int kMaxProblems = 8;           // GEMVs of one grouped launch
 
 // One GEMV of a launch.
-struct alignas(64) Prob {
+struct Prob {
   CUtensorMap tm_codes;       // codes plane as a 2-D u8 tensor {code bytes per row, n}, box 128 x 128
   CUtensorMap tm_scales;      // scales plane as a 2-D u16 tensor {G, n}, box 8 x 128 (if scales_tma)
   const uint16_t* scales;
@@ -613,23 +613,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 }
 
 // ----------------------------------------------------------------------------- host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
 int pad_batch(int b) { return b <= 1 ? 1 : b <= 2 ? 2 : b <= 4 ? 4 : 8; }
 
 // Split of K across a cluster (S CTAs, chunk of gpc groups) from a simple time model: every CTA
@@ -682,7 +665,7 @@ template <int FMT>
 lb_status encode_maps(const lb_weight& W, CUtensorMap& tm_codes, CUtensorMap& tm_scales, int scales_tma) {
   const int n = static_cast<int>(W.n), k = static_cast<int>(W.k), G = k / lb::kGroup;
   const int gbytes = FmtTraits<FMT>::gbytes;
-  EncodeTiledFn enc = encode_fn();
+  lb::EncodeTiledFn enc = lb::tensor_map_encoder();
   if (!enc) return lb::fail(LB_ERR_CUDA, "lb_gemv: cuTensorMapEncodeTiled unavailable");
   {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k) * gbytes / 128, static_cast<cuuint64_t>(n)};
@@ -881,6 +864,19 @@ lb_status launch_mb(const lb_gemv_problem* probs, int count, int batch, cudaStre
 }  // namespace
 
 namespace lb {
+
+EncodeTiledFn tensor_map_encoder() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
 
 lb_status launch_gemv(const lb_weight& W, const void* x, int xdt, int batch, void* y, cudaStream_t st) {
   const uint16_t* xs = static_cast<const uint16_t*>(x);

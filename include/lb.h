@@ -172,7 +172,7 @@ lb_status lb_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, int xdt, size
  *     Y[r][n] = sum_g s[n][g] * sum_{i<128} t[n][128g+i] * X[r][128g+i],   0 <= r < m,
  * FP32 accumulation on the tensor cores, output rounded to `ydt` (RNE).
  *
- * W                : packed matrix (n x k); n must be a multiple of 16.
+ * W                : packed matrix (n x k), 1-bit or ternary; n must be a multiple of 16.
  * x                : device [m][k] of `xdt`, 16-byte aligned.  Values must lie in the binary16
  *                    range |x| <= 65504 (the product runs on FP16 tensor-core operands, where
  *                    s * t is exact); bfloat16 inputs are converted to binary16 first.
@@ -180,7 +180,9 @@ lb_status lb_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, int xdt, size
  * workspace        : device scratch of at least lb_gemm_workspace_bytes(...) bytes, 256-byte
  *                    aligned, used only during this call's kernels (may be reused afterwards).
  * Asynchronous on `stream`.  Errors (no launch): LB_ERR_NULL, LB_ERR_SHAPE, LB_ERR_ALIGN,
- * LB_ERR_DTYPE, LB_ERR_WORKSPACE; LB_ERR_UNSUPPORTED for the 1-bit format; LB_ERR_CUDA.
+ * LB_ERR_DTYPE, LB_ERR_WORKSPACE; LB_ERR_CUDA.  Any m is served by the same kernels: a token tile
+ * holding fewer than 256 tokens runs its tensor-core products only as wide as its token count
+ * (rounded up to 16), so mid-size m (16 .. 128) pays for the tokens it has.
  */
 lb_status lb_gemm(const lb_weight* W, const void* x, int xdt, int64_t m, void* y, int ydt,
                   void* workspace, size_t workspace_bytes, lb_stream stream);

@@ -92,8 +92,8 @@ def test_gemm_validation():
     assert _status(lb.lb_gemm, W, A16, lb.LB_BF16, 0, A16, lb.LB_BF16, A16, need, 0) == "LB_ERR_SHAPE"
     assert _status(lb.lb_gemm, lb.make_weight(2, 250, 256, A16, A16), A16, lb.LB_BF16, 5, A16, lb.LB_BF16,
                    A16, need, 0) == "LB_ERR_SHAPE"
-    assert _status(lb.lb_gemm, lb.make_weight(1, 256, 256, A16, A16), A16, lb.LB_BF16, 5, A16, lb.LB_BF16,
-                   A16, need, 0) == "LB_ERR_UNSUPPORTED"
+    assert _status(lb.lb_gemm, lb.make_weight(1, 250, 256, A16, A16), A16, lb.LB_BF16, 5, A16, lb.LB_BF16,
+                   A16, need, 0) == "LB_ERR_SHAPE"
     assert _status(lb.lb_gemm, W, A16, 5, 5, A16, lb.LB_BF16, A16, need, 0) == "LB_ERR_DTYPE"
 
 
