@@ -118,6 +118,43 @@ def f64_to_f16_bits_rne(values) -> np.ndarray:
     return out.astype(np.uint16)
 
 
+def f64_to_bf16_bits_rne(values) -> np.ndarray:
+    """Round float64 values to bfloat16 with round-to-nearest, ties to even.
+
+    bfloat16: 8 significant bits, exponent bias 127, normal minimum 2^-126, subnormal spacing
+    2^-133, largest finite (2 - 2^-7) * 2^127.  Intended for values exactly representable in
+    float64 (binary16 and float32 values are).  NaN maps to 0x7FC0; overflow to +/-infinity.
+    """
+    v = np.asarray(values, dtype=np.float64)
+    neg = np.signbit(v)
+    a = np.abs(v)
+    finite = np.isfinite(a)
+    _, e2 = np.frexp(np.where(finite & (a > 0), a, 1.0))
+    e = e2.astype(np.int64) - 1                                # a in [2**e, 2**(e+1))
+    subn = a < 2.0 ** -126
+    q_sub = np.rint(np.where(finite & subn, a, 0.0) * 2.0 ** 133)   # multiples of 2**-133
+    q_nrm = np.rint(np.where(finite, a, 0.0) * np.exp2((7 - e).astype(np.float64)))
+    carry = q_nrm >= 256.0
+    e_n = np.where(carry, e + 1, e)
+    q_n = np.where(carry, 128.0, q_nrm)
+    nrm_bits = ((e_n + 127) << 7) | (q_n.astype(np.int64) - 128)
+    nrm_bits = np.where(e_n + 127 >= 255, 0x7F80, nrm_bits)
+    out = np.where(subn, q_sub.astype(np.int64), nrm_bits)    # q_sub == 128 is 2**-126
+    out = np.where(np.isinf(a), 0x7F80, out)
+    out = np.where(np.isnan(a), 0x7FC0, out)
+    out = np.where(neg & ~np.isnan(a), out | 0x8000, out)
+    return out.astype(np.uint16)
+
+
+def encode_output_bits(values, dtype: str) -> np.ndarray:
+    """float64 -> 16-bit patterns of 'f16' or 'bf16', round-to-nearest-even."""
+    if dtype == "f16":
+        return f64_to_f16_bits_rne(values)
+    if dtype == "bf16":
+        return f64_to_bf16_bits_rne(values)
+    raise OracleError("dtype", f"unknown output dtype {dtype!r}")
+
+
 def decode_activation_bits(bits, dtype: str) -> np.ndarray:
     """x or y stored as 16-bit patterns -> float64.  dtype is 'f16' or 'bf16'."""
     if dtype == "f16":
@@ -233,6 +270,30 @@ def dequantize(fmt: int, codes, scales, k: int) -> np.ndarray:
         raise OracleError("format", f"unknown format {fmt}")
     s = f16_bits_to_f64(np.asarray(scales, dtype=np.uint16))
     return t.astype(np.float64) * np.repeat(s, GROUP, axis=1)
+
+
+# ---------------------------------------------------------------------------------------
+# Embedding rows.  The low-bit representation also covers the embedding table ([P2] "Cómo
+# funciona la compresión"; [P4] es.news.hada.io topic 31450, "Configuración multimodal y de bajo
+# bit de extremo a extremo"), so the step before the first GEMV dequantises one table row per
+# token: out[i][k] = s[id_i][k // 128] * t[id_i][k], rounded to the output format.
+# ---------------------------------------------------------------------------------------
+
+def embed_rows(fmt: int, codes, scales, k: int, ids, out_dtype: str) -> tuple[np.ndarray, np.ndarray]:
+    """ids int [count] -> (out 16-bit patterns [count][K], bad bool [count]).
+
+    A row id outside [0, N) is not a table row: its output row is all +0 and it is flagged.
+    """
+    codes = np.asarray(codes, dtype=np.uint8)
+    scales = np.asarray(scales, dtype=np.uint16)
+    n = codes.shape[0]
+    ids = np.asarray(ids, dtype=np.int64).reshape(-1)
+    bad = (ids < 0) | (ids >= n)
+    rows = np.where(bad, 0, ids)
+    w = dequantize(fmt, codes[rows], scales[rows], k) if len(ids) else np.zeros((0, k))
+    out = encode_output_bits(w, out_dtype)
+    out[bad] = 0
+    return out, bad
 
 
 # ---------------------------------------------------------------------------------------

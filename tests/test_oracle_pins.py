@@ -68,6 +68,64 @@ def pin_f16_encode():
     assert np.array_equal(orc.f64_to_f16_bits_rne(f32.astype(np.float64)), lib)
 
 
+def pin_bf16_encode():
+    # every finite bfloat16 value maps back to its own pattern
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    vals = orc.bf16_bits_to_f64(bits)
+    fin = np.isfinite(vals)
+    assert np.array_equal(orc.f64_to_bf16_bits_rne(vals[fin]), bits[fin])
+    # ties, quarter points and the overflow edge, against torch's float32 -> bfloat16 conversion
+    pos = np.sort(np.unique(np.abs(vals[fin])))
+    mids = np.concatenate([(pos[:-1] + pos[1:]) / 2, pos[:-1] * 0.75 + pos[1:] * 0.25])
+    top = float(pos[-1])
+    mids = np.concatenate([mids, -mids, [top * (1 + 2.0 ** -9), top * (1 + 2.0 ** -8) * 0.999999]])
+    mids = mids[np.abs(mids) < 3.4e38]                     # float32-representable inputs
+    lib = torch.from_numpy(mids.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    ours = orc.f64_to_bf16_bits_rne(mids.astype(np.float32).astype(np.float64))
+    assert np.array_equal(ours, lib), f"RNE differs at {mids[ours != lib][:5]}"
+    # a dense random sweep of float32 inputs across the exponent range (subnormals included)
+    rng = np.random.default_rng(8)
+    f32 = (rng.standard_normal(200000) * np.exp2(rng.integers(-140, 120, 200000))).astype(np.float32)
+    lib = torch.from_numpy(f32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(orc.f64_to_bf16_bits_rne(f32.astype(np.float64)), lib)
+
+
+def pin_embed():
+    """Embedding rows against the raw inputs, with numpy's binary16 and torch's bfloat16
+    arithmetic: a 1-bit row is sign(w) * fp16(max |w| of the group); a ternary row is t * s."""
+    rng = np.random.default_rng(9)
+    n, k = 37, 384
+    w = (rng.standard_normal((n, k)) * 0.1).astype(np.float32)
+    w[3, :128] = 0.0                                       # an all-zero group: s = 0, bits 1 -> +0
+    codes, scales = orc.pack_1bit(w)
+    ids = np.array([5, 0, 36, 3, 5, -1, 37, 12])
+    s_ref = np.abs(w).reshape(n, k // 128, 128).max(axis=2).astype(np.float16)       # numpy RNE
+    for dt in ("f16", "bf16"):
+        out, bad = orc.embed_rows(orc.FMT_1BIT, codes, scales, k, ids, dt)
+        assert bad.tolist() == [False] * 5 + [True, True, False]
+        assert not out[bad].any()
+        for r, i in enumerate(ids):
+            if bad[r]:
+                continue
+            v = np.where(w[i] >= 0, 1.0, -1.0).astype(np.float16) * np.repeat(s_ref[i], 128)
+            if dt == "f16":
+                exp = v.view(np.uint16)
+            else:
+                exp = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+            assert np.array_equal(out[r], exp), (dt, r)
+    t = rng.integers(-1, 2, (n, k)).astype(np.int8)
+    sb = (np.abs(rng.standard_normal((n, k // 128))) * 0.02).astype(np.float16)
+    sb[7, 1] = -sb[7, 1]                                   # a negative scale: t = 0 gives -0
+    codes, scales = orc.pack_ternary(t, sb.view(np.uint16))
+    ids = np.array([7, 7, 0, 36])
+    out, bad = orc.embed_rows(orc.FMT_TERNARY, codes, scales, k, ids, "f16")
+    assert not bad.any()
+    for r, i in enumerate(ids):
+        exp = (t[i].astype(np.float16) * np.repeat(sb[i], 128)).view(np.uint16)
+        assert np.array_equal(out[r], exp), r
+    assert (out[0, 128:256][t[7, 128:256] == 0] == 0x8000).all()
+
+
 # --------------------------------------------------------------------------- sizes
 
 def pin_sizes():
@@ -334,7 +392,8 @@ def pin_tolerance_rule():
                                     "bf16").any()
 
 
-ALL_PINS = [pin_f16_decode_exhaustive, pin_bf16_decode_exhaustive, pin_f16_encode, pin_sizes,
+ALL_PINS = [pin_f16_decode_exhaustive, pin_bf16_decode_exhaustive, pin_f16_encode, pin_bf16_encode, pin_embed,
+            pin_sizes,
             pin_demo_group, pin_layout_fixtures, pin_roundtrip_1bit, pin_roundtrip_ternary,
             pin_rowsum_invariant, pin_unit_vectors, pin_bruteforce_exact,
             pin_linearity_and_scaling, pin_errors, pin_tolerance_rule]
@@ -422,8 +481,26 @@ def _mut_rne_truncate(monkeypatch):
     monkeypatch.setattr(orc, "f64_to_f16_bits_rne", bad)
 
 
+def _mut_bf16_truncate(monkeypatch):
+    real = orc.f64_to_bf16_bits_rne
+
+    def bad(v):
+        v = np.asarray(v, dtype=np.float64)
+        return real(np.where(np.abs(v) > 0, v * (1 - 2.0 ** -9), v))      # biased toward zero
+    monkeypatch.setattr(orc, "f64_to_bf16_bits_rne", bad)
+
+
+def _mut_embed_row_offset(monkeypatch):
+    real = orc.embed_rows
+
+    def bad(fmt, codes, scales, k, ids, out_dtype):
+        return real(fmt, codes, scales, k, np.asarray(ids) + 1, out_dtype)   # off-by-one row
+    monkeypatch.setattr(orc, "embed_rows", bad)
+
+
 MUTATIONS = [_mut_bitorder_big, _mut_sign_strict, _mut_scale_mean, _mut_ternary_field,
-             _mut_drop_scale, _mut_scale_axis, _mut_f16_bias, _mut_abs_sum, _mut_rne_truncate]
+             _mut_drop_scale, _mut_scale_axis, _mut_f16_bias, _mut_abs_sum, _mut_rne_truncate,
+             _mut_bf16_truncate, _mut_embed_row_offset]
 
 
 @pytest.mark.parametrize("mutation", MUTATIONS, ids=lambda m: m.__name__)
