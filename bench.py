@@ -379,6 +379,31 @@ def measure_gemm_row(lbt, peaks, sel=None):
     return rows
 
 
+def measure_embed_rows(lbt, peaks, sel=None):
+    """Embedding-row gather from the 1-bit 151936 x 2048 table: 32768 token ids (a long prefill),
+    bfloat16 rows out (134 MB, larger than L2)."""
+    name = "embed_c3_1bit_bf16_32k"
+    if not _want(name, sel):
+        return {}
+    wl = synth.WORKLOADS["c3"]
+    pw = _pack_workload(wl, lbt)[0]
+    count = 32768
+    g = torch.Generator().manual_seed(2024)
+    ids = torch.randint(0, pw.n, (count,), generator=g, dtype=torch.int32).cuda()
+    out = torch.empty(count, pw.k, dtype=torch.bfloat16, device="cuda")
+    reps = 8
+    gr = _graph(lambda: [lbt.embed(pw, ids, torch.bfloat16, out) for _ in range(reps)])
+    _time_graph(gr)
+    ms = _time_graph(gr, reps=3) / reps
+    row_in = pw.k // 8 + 2 * (pw.k // 128)
+    by = count * (row_in + 4 + 2 * pw.k)
+    gbs = by / (ms * 1e-3) / 1e9
+    return {name: {"table": [pw.n, pw.k], "fmt": "1bit", "tokens": count, "out": "bf16",
+                   "us_per_call": round(ms * 1e3, 2), "GB_s": round(gbs, 1),
+                   "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 3),
+                   "bytes_basis": "codes + scales of each gathered row + ids + rows written"}}
+
+
 def cpu_baseline(seconds: float = 10.0):
     """The oracle as it stands (FP64 numpy) on the headline layer set, repeated for ~seconds."""
     from oracle import lb_oracle as orc
@@ -547,6 +572,7 @@ def run_ours(args, ws, rank, local):
         rows.update(measure_pack_rows(lbt, peaks, sel))
         rows.update(measure_gemv_rows(lbt, peaks, sel))
         rows.update(measure_gemm_row(lbt, peaks, sel))
+        rows.update(measure_embed_rows(lbt, peaks, sel))
     assert lbl.lb_device_error(clear=True) == 0, "device error word set"
 
     if rank != 0:

@@ -1,4 +1,5 @@
 // liblb C ABI: argument validation, error reporting and dispatch to the kernel launchers.
+#include <climits>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -216,6 +217,22 @@ lb_status lb_gemm_noalloc(const lb_weight* W, const void* x, int xdt, int64_t m,
   if (W->n % 16) return fail(LB_ERR_SHAPE, "lb_gemm_noalloc needs n %% 16 == 0 (got %lld)", (long long)W->n);
   if (!lb::aligned16(x) || !lb::aligned16(y)) return fail(LB_ERR_ALIGN, "x and y must be 16-byte aligned");
   return lb::launch_gemm_noalloc(*W, x, xdt, m, y, ydt, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lb_status lb_embed(const lb_weight* W, const int32_t* ids, int64_t count, void* out, int out_dtype,
+                   lb_stream stream) {
+  lb_status s = check_weight(W);
+  if (s != LB_OK) return s;
+  if (count < 0 || count > INT32_MAX) return fail(LB_ERR_SHAPE, "count must be in [0, 2^31) (got %lld)", (long long)count);
+  if (count * ((W->k + 1023) / 1024) > (int64_t(1) << 34))
+    return fail(LB_ERR_SHAPE, "count x K too large for one launch (count %lld, k %lld)", (long long)count,
+                (long long)W->k);
+  if (!valid_dtype(out_dtype)) return fail(LB_ERR_DTYPE, "unknown output dtype %d", out_dtype);
+  if (count == 0) return LB_OK;
+  if (!ids || !out) return fail(LB_ERR_NULL, "ids and out must be non-NULL");
+  if (!lb::aligned16(out) || (reinterpret_cast<uintptr_t>(ids) & 3u))
+    return fail(LB_ERR_ALIGN, "out must be 16-byte aligned and ids 4-byte aligned");
+  return lb::launch_embed(*W, ids, count, out, out_dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
 lb_status lb_device_error(uint32_t* word, int clear) {

@@ -32,6 +32,7 @@ EncodeTiledFn tensor_map_encoder();
 uint32_t* device_error_word();
 constexpr uint32_t kErrGemmTimeout = 1u;        // a GEMM pipeline wait gave up
 constexpr uint32_t kErrGemmInputRange = 2u;     // a GEMM activation did not fit binary16
+constexpr uint32_t kErrEmbedId = 4u;            // an embedding row id outside [0, n)
 
 // Launchers implemented by the kernel translation units.  They assume validated arguments.
 lb_status launch_pack_1bit(const float* w, int64_t n, int64_t k, uint8_t* codes, uint16_t* scales,
@@ -43,6 +44,8 @@ lb_status launch_gemv_batched(const lb_gemv_problem* probs, int count, int xdt, 
 size_t gemm_workspace_bytes(int64_t m, int64_t k);
 lb_status launch_gemm(const lb_weight& W, const void* x, int xdt, int64_t m, void* y, int ydt,
                       void* ws, cudaStream_t st);
+lb_status launch_embed(const lb_weight& W, const int32_t* ids, int64_t count, void* out, int out_dtype,
+                       cudaStream_t st);
 lb_status launch_gemm_noalloc(const lb_weight& W, const void* x, int xdt, int64_t m, void* y, int ydt,
                               cudaStream_t st);
 

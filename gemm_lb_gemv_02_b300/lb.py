@@ -30,7 +30,7 @@ STATUS_NAMES = {0: "LB_OK", 1: "LB_ERR_NULL", 2: "LB_ERR_SHAPE", 3: "LB_ERR_ALIG
 # Symbols declared in include/lb.h (checked by the tests against the header and the library).
 EXPORTED = ("lb_status_string", "lb_last_error", "lb_version", "lb_packed_bytes", "lb_pack_1bit",
             "lb_pack_ternary", "lb_gemv", "lb_gemm_workspace_bytes", "lb_gemm", "lb_device_error",
-            "lb_gemm_noalloc", "lb_gemv_batched")
+            "lb_gemm_noalloc", "lb_gemv_batched", "lb_embed")
 LB_GEMM_NOALLOC_SCRATCH_BYTES = 8 << 20
 LB_GEMV_BATCH_MAX = 8
 
@@ -71,6 +71,7 @@ def _load():
         "lb_device_error": ([ctypes.POINTER(ctypes.c_uint32), i32], i32),
         "lb_gemm_noalloc": ([ctypes.POINTER(lb_weight), vp, i32, i64, vp, i32, vp], i32),
         "lb_gemv_batched": ([ctypes.POINTER(lb_gemv_problem), i32, i32, i32, vp], i32),
+        "lb_embed": ([ctypes.POINTER(lb_weight), vp, i64, vp, i32, vp], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -180,6 +181,11 @@ def lb_gemm(W: lb_weight, x, xdt: int, m: int, y, ydt: int, workspace, workspace
 def lb_gemm_noalloc(W: lb_weight, x, xdt: int, m: int, y, ydt: int, stream=None) -> None:
     """lb_gemm without a workspace: the library stages activations in its own static scratch."""
     _check(_lib.lb_gemm_noalloc(ctypes.byref(W), _ptr(x), xdt, m, _ptr(y), ydt, _stream(stream)), "lb_gemm_noalloc")
+
+
+def lb_embed(W: lb_weight, ids, count: int, out, out_dtype: int, stream=None) -> None:
+    """Embedding rows out[i] = dequantised row ids[i] of W (ids: int32 device tensor)."""
+    _check(_lib.lb_embed(ctypes.byref(W), _ptr(ids), count, _ptr(out), out_dtype, _stream(stream)), "lb_embed")
 
 
 def lb_device_error(clear: bool = False) -> int:

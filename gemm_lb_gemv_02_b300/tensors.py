@@ -101,3 +101,15 @@ def gemm(W: PackedWeight, x: torch.Tensor, out_dtype: torch.dtype = torch.bfloat
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
     lb.lb_gemm(W.struct(), x, xdt, m, y, dtype_code(y.dtype), workspace, workspace.numel(), stream)
     return y
+
+
+def embed(W: PackedWeight, ids: torch.Tensor, out_dtype: torch.dtype = torch.bfloat16,
+          out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Embedding rows out[i] = dequantised row ids[i] of the packed table W (ids: int32 CUDA tensor)."""
+    assert ids.is_cuda and ids.dtype == torch.int32 and ids.is_contiguous() and ids.dim() == 1
+    count = ids.shape[0]
+    if out is None:
+        out = torch.empty(count, W.k, dtype=out_dtype, device=ids.device)
+    assert out.is_cuda and out.is_contiguous() and out.shape == (count, W.k)
+    lb.lb_embed(W.struct(), ids, count, out, dtype_code(out.dtype), stream)
+    return out

@@ -188,10 +188,32 @@ lb_status lb_gemm(const lb_weight* W, const void* x, int xdt, int64_t m, void* y
                   void* workspace, size_t workspace_bytes, lb_stream stream);
 
 /*
+ * Embedding-row gather (7minutos.es, "PrismML lanza Bonsai 27B", section "Cómo funciona la
+ * compresión", and es.news.hada.io topic 31450, section "Configuración multimodal y de bajo bit
+ * de extremo a extremo": the low-bit representation covers the embedding table too):
+ *     out[i][k] = s[ids[i]][k / 128] * t[ids[i]][k],   0 <= i < count, 0 <= k < K,
+ * rounded to `out_dtype` (RNE; binary16 output is exact, bfloat16 output rounds the scale once).
+ * t = 0 gives a zero carrying the sign of s, as IEEE multiplication does.
+ *
+ * W         : packed table (N rows x K), either format.
+ * ids       : device int32 [count] row ids, 4-byte aligned.  An id outside [0, N) is not a
+ *             table row: its output row is written as +0 and bit 2 of the device error word is
+ *             set (lb_device_error); the call itself cannot see device data and returns LB_OK.
+ * count     : 0 .. 2^31 - 1 rows with count * ceil(K / 1024) <= 2^34; 0 launches nothing (ids
+ *             and out may then be NULL).
+ * out       : device [count][K] of `out_dtype`, 16-byte aligned, caller-owned.
+ * Asynchronous on `stream`.  Errors (no launch): LB_ERR_NULL, LB_ERR_SHAPE, LB_ERR_ALIGN,
+ * LB_ERR_DTYPE (format or out_dtype), LB_ERR_CUDA if the launch fails.
+ */
+lb_status lb_embed(const lb_weight* W, const int32_t* ids, int64_t count, void* out, int out_dtype,
+                   lb_stream stream);
+
+/*
  * Sticky device-side error word of the current device (0 = none).  Kernels that wait on an
  * mbarrier give up after a bounded number of polls, set a bit here and return instead of
  * hanging.  lb_device_error() synchronises the device, reads the word and, if `clear` is
- * non-zero, resets it.  Bit 0: a GEMM pipeline wait timed out.
+ * non-zero, resets it.  Bit 0: a GEMM pipeline wait timed out.  Bit 1: a GEMM activation lay
+ * outside the binary16 range.  Bit 2: an lb_embed row id lay outside [0, n).
  */
 lb_status lb_device_error(uint32_t* word, int clear);
 

@@ -97,6 +97,22 @@ def test_gemm_validation():
     assert _status(lb.lb_gemm, W, A16, 5, 5, A16, lb.LB_BF16, A16, need, 0) == "LB_ERR_DTYPE"
 
 
+def test_embed_validation():
+    W = lb.make_weight(lb.LB_FMT_1BIT_G128, 64, 256, A16, A16)
+    assert _status(lb.lb_embed, W, A16, 0, None, lb.LB_BF16, 0) == "LB_OK"            # nothing to do
+    assert _status(lb.lb_embed, W, A16, -1, A16, lb.LB_BF16, 0) == "LB_ERR_SHAPE"
+    assert _status(lb.lb_embed, W, A16, 2 ** 31, A16, lb.LB_BF16, 0) == "LB_ERR_SHAPE"
+    wide = lb.make_weight(lb.LB_FMT_1BIT_G128, 64, 1 << 24, A16, A16)                # 16384 pieces per row
+    assert _status(lb.lb_embed, wide, A16, 2 ** 20 + 1, A16, lb.LB_BF16, 0) == "LB_ERR_SHAPE"
+    assert _status(lb.lb_embed, W, None, 3, A16, lb.LB_BF16, 0) == "LB_ERR_NULL"
+    assert _status(lb.lb_embed, W, A16, 3, None, lb.LB_BF16, 0) == "LB_ERR_NULL"
+    assert _status(lb.lb_embed, W, A16, 3, A16, 7, 0) == "LB_ERR_DTYPE"
+    assert _status(lb.lb_embed, W, A16 + 2, 3, A16, lb.LB_F16, 0) == "LB_ERR_ALIGN"     # ids: 4-byte
+    assert _status(lb.lb_embed, W, A16, 3, A16 + 8, lb.LB_F16, 0) == "LB_ERR_ALIGN"     # out: 16-byte
+    assert _status(lb.lb_embed, lb.make_weight(3, 64, 256, A16, A16), A16, 3, A16, lb.LB_F16, 0) == "LB_ERR_DTYPE"
+    assert _status(lb.lb_embed, lb.make_weight(2, 64, 200, A16, A16), A16, 3, A16, lb.LB_F16, 0) == "LB_ERR_SHAPE"
+
+
 def test_gemv_batched_validation():
     W1 = lb.make_weight(lb.LB_FMT_1BIT_G128, 16, 128, A16, A16)
     Wt = lb.make_weight(lb.LB_FMT_TERNARY_G128, 16, 128, A16, A16)

@@ -6,7 +6,7 @@ import torch
 
 from gemm_lb_gemv_02_b300 import synth
 from oracle import lb_oracle as orc
-from tests.helpers import check_products, oracle_pack, u16, u8
+from tests.helpers import check_products, oracle_pack, u16
 
 pytestmark = pytest.mark.gpu
 
@@ -93,8 +93,7 @@ def test_gemm_c5_prefill_sampled():
     inp = synth.matrix_inputs(wl, 0)
     pw = tensors.pack_ternary(inp["t"].cuda(), inp["s"].cuda())
     x = synth.workload_activations(wl, 0, 512)
-    codes = u8(pw.codes).reshape(mat.n, -1)
-    scales = u16(pw.scales).reshape(mat.n, -1)
+    codes, scales = oracle_pack("ternary", inp)
     rng = np.random.default_rng(5)
     rows = np.unique(np.concatenate([[0, 127, 128, 511], rng.integers(0, 512, 92)]))
     cols = np.unique(np.concatenate([np.arange(8), np.arange(mat.n - 8, mat.n), rng.integers(0, mat.n, 1184)]))
@@ -110,8 +109,7 @@ def test_gemm_1bit_block_prefill_sampled():
     inp = synth.matrix_inputs(wl, idx)
     pw = tensors.pack_1bit(inp["w"].cuda())
     x = synth.workload_activations(wl, idx, 512)
-    codes = u8(pw.codes).reshape(mat.n, -1)
-    scales = u16(pw.scales).reshape(mat.n, -1)
+    codes, scales = oracle_pack("1bit", inp)
     rng = np.random.default_rng(6)
     rows = np.unique(np.concatenate([[0, 255, 256, 511], rng.integers(0, 512, 60)]))
     cols = np.unique(np.concatenate([np.arange(8), np.arange(mat.n - 8, mat.n), rng.integers(0, mat.n, 600)]))

@@ -6,7 +6,7 @@ import torch
 
 from gemm_lb_gemv_02_b300 import synth
 from oracle import lb_oracle as orc
-from tests.helpers import check_products, oracle_pack, oracle_products, u16, u8
+from tests.helpers import check_products, oracle_pack, oracle_products, u16
 
 pytestmark = pytest.mark.gpu
 
@@ -96,10 +96,13 @@ def _workload_check(key, batch, sample_rows=None):
             rng = np.random.default_rng(i)
             rows = np.unique(np.concatenate([np.arange(16), np.arange(mat.n - 16, mat.n),
                                              rng.integers(0, mat.n, sample_rows)]))
-        # the oracle works from the device-packed planes (their bit-exactness is tested separately)
-        codes = u8(pw.codes).reshape(mat.n, -1)
-        scales = u16(pw.scales).reshape(mat.n, -1)
-        y_ref, a = oracle_products(wl.fmt, codes, scales, mat.k, x.cpu(), rows)
+        # the oracle packs the checked rows itself from the raw inputs (packing is row by row)
+        sel = slice(None) if rows is None else rows
+        if wl.fmt == "1bit":
+            codes, scales = orc.pack_1bit(inp["w"].numpy()[sel])
+        else:
+            codes, scales = orc.pack_ternary(inp["t"].numpy()[sel], inp["s"].numpy().view(np.uint16)[sel])
+        y_ref, a = oracle_products(wl.fmt, codes, scales, mat.k, x.cpu())
         worst = max(worst, check_products(y, y_ref, a, f"{key}/{mat.name} batch={batch}", cols=rows))
         del pw, x, y
     return worst
@@ -155,7 +158,7 @@ def test_gemv_batched_c2_layer_set_grouping():
     mats = {}
     for i, mat in enumerate(wl.matrices):
         inp = synth.matrix_inputs(wl, i)
-        mats[mat.name] = (tensors.pack_ternary(inp["t"].cuda(), inp["s"].cuda()), mat)
+        mats[mat.name] = (tensors.pack_ternary(inp["t"].cuda(), inp["s"].cuda()), mat, oracle_pack("ternary", inp))
     x_attn = synth.activations(1, 2048, "f16", seed=71).cuda()
     x_o = synth.activations(1, 2048, "f16", seed=72).cuda()
     x_ffn = synth.activations(1, 2048, "f16", seed=73).cuda()
@@ -166,9 +169,7 @@ def test_gemv_batched_c2_layer_set_grouping():
         ys = tensors.gemv_batched([(mats[name][0], x) for name, x in grp])
         torch.cuda.synchronize()
         for (name, x), y in zip(grp, ys):
-            pw, mat = mats[name]
-            codes = u8(pw.codes).reshape(mat.n, -1)
-            scales = u16(pw.scales).reshape(mat.n, -1)
+            pw, mat, (codes, scales) = mats[name]
             y_ref, a = oracle_products("ternary", codes, scales, mat.k, x.cpu())
             check_products(y, y_ref, a, f"c2/{name} grouped")
 
