@@ -317,6 +317,46 @@ def gemm(fmt: int, codes, scales, k: int, x: np.ndarray) -> tuple[np.ndarray, np
     return matvec(fmt, codes, scales, k, x)
 
 
+# ---------------------------------------------------------------------------------------
+# SiLU-gated feed-forward pair: h = silu(W_gate x) * (W_up x).  The pages name the fastest decode
+# kernels as specialised at the matvec / FFN level ([P5] "Detalles técnicos") and the models as
+# builds of a Qwen3-family base ([P2]), whose feed-forward block gates the up projection with
+# silu(z) = z * sigmoid(z) = z / (1 + e^-z) of the gate projection.
+# ---------------------------------------------------------------------------------------
+
+SILU_SLOPE_MAX = 1.0999     # bounds max over z of |d/dz silu(z)| = 1.09984 (near z = 2.40)
+
+
+def silu(z) -> np.ndarray:
+    """z / (1 + e^-z) in float64; e^-z overflowing to infinity gives the limit, a signed zero."""
+    z = np.asarray(z, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
+
+
+def swiglu(fmt: int, codes_g, scales_g, codes_u, scales_u, k: int, x: np.ndarray):
+    """x float64 [B][K] -> (h [B][N], g, a_g, u, a_u): h = silu(g) * u with g, u the two products
+    and a_g, a_u their sums of absolute terms (for the tolerance)."""
+    g, a_g = matvec(fmt, codes_g, scales_g, k, x)
+    u, a_u = matvec(fmt, codes_u, scales_u, k, x)
+    return silu(g) * u, g, a_g, u, a_u
+
+
+def swiglu_tolerance(h_ref, g, a_g, u, a_u, h_test=None, out_dtype: str | None = None) -> np.ndarray:
+    """Allowed |h_test - h_ref| when g and u are each FP32-accumulated within the product bound
+    dg = 2e-3 * a_g + 1e-5, du = 2e-3 * a_u + 1e-5 and h is formed from them in FP32:
+    |silu(g') u' - silu(g) u| <= SILU_SLOPE_MAX * dg * (|u| + du) + |silu(g)| * du, plus 1e-6 |h|
+    for the FP32 evaluation of silu and the product, plus half an ulp of the output format."""
+    dg = TOL_REL * np.asarray(a_g) + TOL_ABS
+    du = TOL_REL * np.asarray(a_u) + TOL_ABS
+    h_ref = np.asarray(h_ref, dtype=np.float64)
+    mag = np.abs(h_ref)
+    if h_test is not None:
+        mag = np.maximum(mag, np.abs(np.asarray(h_test, dtype=np.float64)))
+    return (SILU_SLOPE_MAX * dg * (np.abs(u) + du) + np.abs(silu(g)) * du + 1e-6 * mag
+            + output_half_ulp(mag, out_dtype))
+
+
 def output_half_ulp(v, dtype: str | None) -> np.ndarray:
     """Half a unit in the last place of the output format at magnitude |v| (0 if dtype is None).
 

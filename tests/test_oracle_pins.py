@@ -126,6 +126,55 @@ def pin_embed():
     assert (out[0, 128:256][t[7, 128:256] == 0] == 0x8000).all()
 
 
+def pin_silu():
+    """silu against 50-digit mpmath, its limits, and the slope constant of the SwiGLU bound."""
+    import mpmath
+    mpmath.mp.dps = 50
+    z = np.concatenate([np.linspace(-60, 60, 2401), [0.0, -0.0, 1e-300, -1e-300, 700.0, -700.0, 800.0, -800.0]])
+    ours = orc.silu(z)
+    ref = np.array([float(mpmath.mpf(float(v)) / (1 + mpmath.exp(-mpmath.mpf(float(v))))) for v in z])
+    assert np.allclose(ours, ref, rtol=1e-14, atol=0.0), np.max(np.abs(ours - ref) / np.maximum(np.abs(ref), 1e-300))
+    # the limits, reached at finite arguments (a product of finite binary16 inputs stays finite)
+    assert orc.silu(np.array([800.0]))[0] == 800.0 and orc.silu(np.array([-800.0]))[0] == 0.0
+    assert orc.silu(np.array([np.log(3.0)]))[0] == pytest.approx(0.75 * np.log(3.0), rel=1e-15)
+    # the slope of silu: sigma(z) (1 + z (1 - sigma(z))); its maximum is the constant of the bound
+    zz = np.linspace(-20, 20, 400001)
+    sg = 1.0 / (1.0 + np.exp(-zz))
+    slope = np.abs(sg * (1.0 + zz * (1.0 - sg)))
+    assert slope.max() <= orc.SILU_SLOPE_MAX and slope.max() > orc.SILU_SLOPE_MAX - 1e-4
+
+
+def pin_swiglu():
+    """A tiny pair by brute force from the raw inputs in 50-digit arithmetic, and the tolerance
+    bound checked at the corners of the allowed product errors."""
+    import mpmath
+    mpmath.mp.dps = 50
+    rng = np.random.default_rng(10)
+    n, k, b = 3, 256, 2
+    tg = rng.integers(-1, 2, (n, k)).astype(np.int8)
+    tu = rng.integers(-1, 2, (n, k)).astype(np.int8)
+    sg = (np.abs(rng.standard_normal((n, k // 128))) * 0.05).astype(np.float16)
+    su = (np.abs(rng.standard_normal((n, k // 128))) * 0.05).astype(np.float16)
+    x = rng.standard_normal((b, k)).astype(np.float16).astype(np.float64)
+    cg, scg = orc.pack_ternary(tg, sg.view(np.uint16))
+    cu, scu = orc.pack_ternary(tu, su.view(np.uint16))
+    h, g, a_g, u, a_u = orc.swiglu(orc.FMT_TERNARY, cg, scg, cu, scu, k, x)
+    for bi in range(b):
+        for r in range(n):
+            gm = sum(mpmath.mpf(float(sg[r, i // 128])) * int(tg[r, i]) * mpmath.mpf(x[bi, i]) for i in range(k))
+            um = sum(mpmath.mpf(float(su[r, i // 128])) * int(tu[r, i]) * mpmath.mpf(x[bi, i]) for i in range(k))
+            hm = gm / (1 + mpmath.exp(-gm)) * um
+            assert abs(h[bi, r] - float(hm)) <= 1e-12 * max(1.0, abs(float(hm))), (bi, r)
+    # perturb g and u to the corners of their product bounds: the bound still holds
+    dg = orc.TOL_REL * a_g + orc.TOL_ABS
+    du = orc.TOL_REL * a_u + orc.TOL_ABS
+    tol = orc.swiglu_tolerance(h, g, a_g, u, a_u)
+    for sgn_g in (-1, 1):
+        for sgn_u in (-1, 1):
+            hp = orc.silu(g + sgn_g * dg) * (u + sgn_u * du)
+            assert (np.abs(hp - h) <= tol).all()
+
+
 # --------------------------------------------------------------------------- sizes
 
 def pin_sizes():
@@ -393,6 +442,7 @@ def pin_tolerance_rule():
 
 
 ALL_PINS = [pin_f16_decode_exhaustive, pin_bf16_decode_exhaustive, pin_f16_encode, pin_bf16_encode, pin_embed,
+            pin_silu, pin_swiglu,
             pin_sizes,
             pin_demo_group, pin_layout_fixtures, pin_roundtrip_1bit, pin_roundtrip_ternary,
             pin_rowsum_invariant, pin_unit_vectors, pin_bruteforce_exact,
@@ -498,7 +548,19 @@ def _mut_embed_row_offset(monkeypatch):
     monkeypatch.setattr(orc, "embed_rows", bad)
 
 
-MUTATIONS = [_mut_bitorder_big, _mut_sign_strict, _mut_scale_mean, _mut_ternary_field,
+def _mut_silu_sign(monkeypatch):
+    monkeypatch.setattr(orc, "silu", lambda z: np.asarray(z, dtype=np.float64) / (1.0 + np.exp(np.asarray(z, dtype=np.float64))))
+
+
+def _mut_swiglu_swap(monkeypatch):
+    real = orc.swiglu
+
+    def bad(fmt, cg, sg, cu, su, k, x):
+        return real(fmt, cu, su, cg, sg, k, x)                            # gate and up exchanged
+    monkeypatch.setattr(orc, "swiglu", bad)
+
+
+MUTATIONS = [_mut_silu_sign, _mut_swiglu_swap, _mut_bitorder_big, _mut_sign_strict, _mut_scale_mean, _mut_ternary_field,
              _mut_drop_scale, _mut_scale_axis, _mut_f16_bias, _mut_abs_sum, _mut_rne_truncate,
              _mut_bf16_truncate, _mut_embed_row_offset]
 
