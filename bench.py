@@ -379,6 +379,52 @@ def measure_gemm_row(lbt, peaks, sel=None):
     return rows
 
 
+SWIGLU_ROWS = (  # row name, workload, batch
+    ("swiglu_c2_b1", "c2", 1),
+    ("swiglu_c4t_b1", "c4t", 1),
+    ("swiglu_c4t_b5", "c4t", 5),
+)
+
+
+def measure_swiglu_rows(lbt, peaks, sel=None):
+    """The feed-forward gate / up pair: h = silu(W_gate x) * (W_up x) in one fused launch, against
+    the same pair issued as one grouped launch of two GEMVs (g and u written out)."""
+    rows = {}
+    for name, key, b in SWIGLU_ROWS:
+        if not _want(name, sel):
+            continue
+        wl = synth.WORKLOADS[key]
+        idx = [next(i for i, m in enumerate(wl.matrices) if m.name == nm) for nm in ("gate", "up")]
+        base = []
+        for i in idx:
+            inp = synth.matrix_inputs(wl, i)
+            base.append(lbt.pack_1bit(inp["w"].cuda()) if wl.fmt == "1bit"
+                        else lbt.pack_ternary(inp["t"].cuda(), inp["s"].cuda()))
+        per_copy = _gemv_bytes(base[0], b) + _gemv_bytes(base[1], b)
+        copies = _copies_for(per_copy)
+        pairs = [base] + [[_clone(pw) for pw in base] for _ in range(copies - 1)]
+        x = synth.workload_activations(wl, idx[0], b).cuda()
+        n = base[0].n
+        h = torch.empty(b, n, dtype=x.dtype, device="cuda")
+        yg, yu = torch.empty_like(h), torch.empty_like(h)
+        steps = copies * 2
+        g_f = _graph(lambda: [lbt.gemv_swiglu(pairs[i % copies][0], pairs[i % copies][1], x, h) for i in range(steps)])
+        _time_graph(g_f)
+        ms_f = _time_graph(g_f, reps=3) / steps
+        g_u = _graph(lambda: [lbt.gemv_batched([(pairs[i % copies][0], x), (pairs[i % copies][1], x)], [yg, yu])
+                              for i in range(steps)])
+        _time_graph(g_u)
+        ms_u = _time_graph(g_u, reps=3) / steps
+        by = per_copy - 2 * b * base[0].k - 2 * b * n     # x read once, one output vector
+        gbs = by / (ms_f * 1e-3) / 1e9
+        rows[name] = {"shape": [n, base[0].k], "fmt": wl.fmt, "batch": b, "us_per_pair": round(ms_f * 1e3, 2),
+                      "GB_s": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 3),
+                      "unfused_grouped_us": round(ms_u * 1e3, 2), "copies_rotated": copies}
+        del pairs, g_f, g_u
+        torch.cuda.empty_cache()
+    return rows
+
+
 def measure_embed_rows(lbt, peaks, sel=None):
     """Embedding-row gather from the 1-bit 151936 x 2048 table: 32768 token ids (a long prefill),
     bfloat16 rows out (134 MB, larger than L2)."""
@@ -573,6 +619,7 @@ def run_ours(args, ws, rank, local):
         rows.update(measure_gemv_rows(lbt, peaks, sel))
         rows.update(measure_gemm_row(lbt, peaks, sel))
         rows.update(measure_embed_rows(lbt, peaks, sel))
+        rows.update(measure_swiglu_rows(lbt, peaks, sel))
     assert lbl.lb_device_error(clear=True) == 0, "device error word set"
 
     if rank != 0:

@@ -180,6 +180,23 @@ lb_status lb_gemv_batched(const lb_gemv_problem* problems, int count, int xdt, i
   return lb::launch_gemv_batched(problems, count, xdt, batch, reinterpret_cast<cudaStream_t>(stream));
 }
 
+lb_status lb_gemv_swiglu(const lb_weight* Wg, const lb_weight* Wu, const void* x, int xdt, int batch, void* h,
+                         lb_stream stream) {
+  lb_status s = check_weight(Wg);
+  if (s != LB_OK) return s;
+  s = check_weight(Wu);
+  if (s != LB_OK) return s;
+  if (Wg->fmt != Wu->fmt) return fail(LB_ERR_UNSUPPORTED, "gate and up must have the same format");
+  if (Wg->n != Wu->n || Wg->k != Wu->k)
+    return fail(LB_ERR_SHAPE, "gate (%lld x %lld) and up (%lld x %lld) must have the same shape", (long long)Wg->n,
+                (long long)Wg->k, (long long)Wu->n, (long long)Wu->k);
+  if (!x || !h) return fail(LB_ERR_NULL, "x and h must be non-NULL");
+  if (!valid_dtype(xdt)) return fail(LB_ERR_DTYPE, "unknown activation dtype %d", xdt);
+  if (batch < 1 || batch > 8) return fail(LB_ERR_SHAPE, "batch must be in [1, 8] (got %d)", batch);
+  if (!lb::aligned16(x) || !lb::aligned16(h)) return fail(LB_ERR_ALIGN, "x and h must be 16-byte aligned");
+  return lb::launch_gemv_swiglu(*Wg, *Wu, x, xdt, batch, h, reinterpret_cast<cudaStream_t>(stream));
+}
+
 lb_status lb_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, int xdt, size_t* bytes) {
   if (!bytes) return fail(LB_ERR_NULL, "bytes is NULL");
   if (!valid_dtype(xdt)) return fail(LB_ERR_DTYPE, "unknown activation dtype %d", xdt);

@@ -133,6 +133,10 @@ __device__ __forceinline__ void mma_acc(float (&d)[4], uint32_t a0, uint32_t a1,
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// SiLU gate, silu(g) = g * sigmoid(g) = g / (1 + e^-g), in FP32 (expf: CUDA's accurate
+// exponential; e^-g = inf for very negative g gives a signed zero, as the limit does).
+__device__ __forceinline__ float silu(float g) { return g / (1.f + expf(-g)); }
+
 // ----------------------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
@@ -200,6 +204,7 @@ struct Args {
   int count;       // problems; 1 = one GEMV with persistent CTAs, > 1 = one CTA per row block
   int batch;
   int S;           // CTAs per cluster along K (chunk = cluster rank); 1 when count > 1
+  int fuse;        // 1: SiLU-gated pair, p[0] = gate, p[1] = up (same n, k, x); h -> p[0].y
 };
 
 template <int FMT, int BP>
@@ -228,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int pi = 0;                                                    // this CTA's problem
-  for (int i = 1; i < a.count; ++i)
+  for (int i = 1; i < a.count && !a.fuse; ++i)
     if (static_cast<int>(blockIdx.y) >= a.p[i].unit0) pi = i;
   const Prob& P = a.p[pi];
   const uint32_t rank = a.S > 1 ? cluster_rank() : 0u;
@@ -236,10 +241,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   const int g_begin = static_cast<int>(rank) * gpc;
   const int ng = min(gpc, P.G - g_begin);                        // groups of this CTA's chunk (<= 0: none)
   const int nst = (ng + GS - 1) / GS;                            // stages per row block
-  // row blocks of this CTA: rb0, rb0 + rb_stride, ... (grouped launch: exactly one)
+  // row blocks of this CTA: rb0, rb0 + rb_stride, ... (grouped launch: exactly one).  A fused
+  // SiLU-gated pair runs row block rb0 twice: unit 0 on the gate matrix, unit 1 on the up matrix.
   const int rb0 = static_cast<int>(blockIdx.y) - P.unit0;
-  const int rb_stride = a.count > 1 ? P.row_blocks : static_cast<int>(gridDim.y);
-  const int my_rbs = (P.row_blocks - rb0 + rb_stride - 1) / rb_stride;
+  const int rb_stride = a.fuse ? 0 : (a.count > 1 ? P.row_blocks : static_cast<int>(gridDim.y));
+  const int my_rbs = a.fuse ? 2 : (P.row_blocks - rb0 + rb_stride - 1) / rb_stride;
   const int total_st = my_rbs * nst;
   bool ok = true;
 
@@ -258,18 +264,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     if (lane == 0) {
       lbdev::prefetch_tmap(&P.tm_codes);
       if (P.scales_tma) lbdev::prefetch_tmap(&P.tm_scales);
+      if (a.fuse) {
+        lbdev::prefetch_tmap(&a.p[1].tm_codes);
+        if (P.scales_tma) lbdev::prefetch_tmap(&a.p[1].tm_scales);
+      }
       const uint32_t bytes = static_cast<uint32_t>(FT::nb * kBox + (P.scales_tma ? kScaleBox : 0));
       for (int st = 0; st < total_st; ++st) {
         const int s = st % L::stages;
         if (!lbdev::mbar_wait(&empty[s], static_cast<uint32_t>(((st / L::stages) & 1) ^ 1))) { ok = false; break; }
         const int row0 = (rb0 + (st / nst) * rb_stride) * ROWS;
+        const Prob& PU = a.p[a.fuse ? st / nst : pi];              // the matrix of this unit
         const int g0 = g_begin + (st % nst) * GS;
         uint8_t* slot = sm + s * L::slot;
         lbdev::mbar_arrive_expect_tx(&full[s], bytes);
 #pragma unroll
         for (int b = 0; b < FT::nb; ++b)
-          lbdev::tma_load_2d(slot + b * kBox, &P.tm_codes, (g0 + b * (GS / FT::nb)) * FT::gbytes, row0, &full[s]);
-        if (P.scales_tma) lbdev::tma_load_2d(slot + FT::nb * kBox, &P.tm_scales, g0, row0, &full[s]);
+          lbdev::tma_load_2d(slot + b * kBox, &PU.tm_codes, (g0 + b * (GS / FT::nb)) * FT::gbytes, row0, &full[s]);
+        if (P.scales_tma) lbdev::tma_load_2d(slot + FT::nb * kBox, &PU.tm_scales, g0, row0, &full[s]);
       }
     }
     __syncwarp();
@@ -409,6 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     const int c0col = 2 * q, c1col = 2 * q + 1;
     const float f0 = colf[c0col] * mul, f1 = colf[c1col] * mul;   // output factors of my columns
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float gate[4] = {0.f, 0.f, 0.f, 0.f};                         // fused pair, S == 1: the gate outputs
     int s = 0, cstage = 0, i_rb = 0;
     uint32_t ph = 0;
 
@@ -419,14 +431,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
       const uint32_t slot = sm32 + static_cast<uint32_t>(s * L::slot);
       float sa[GH], sb[GH];
       if (!P.scales_tma) {                                        // fallback: scales from L2
+        const Prob& PU = a.p[a.fuse ? i_rb : pi];
         const int row_a = rb * ROWS + ia, row_b = row_a + 8;
 #pragma unroll
         for (int j = 0; j < GH; ++j) {
           sa[j] = 0.f; sb[j] = 0.f;
           if (j < cnt) {
             const int64_t g = g_begin + g0 + j;
-            if (row_a < P.n) sa[j] = __half2float(__ushort_as_half(__ldg(P.scales + static_cast<int64_t>(row_a) * P.G + g)));
-            if (row_b < P.n) sb[j] = __half2float(__ushort_as_half(__ldg(P.scales + static_cast<int64_t>(row_b) * P.G + g)));
+            if (row_a < P.n) sa[j] = __half2float(__ushort_as_half(__ldg(PU.scales + static_cast<int64_t>(row_a) * P.G + g)));
+            if (row_b < P.n) sb[j] = __half2float(__ushort_as_half(__ldg(PU.scales + static_cast<int64_t>(row_b) * P.G + g)));
           }
         }
       }
@@ -559,17 +572,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
           const float v1 = (acc[1] + red[ia * 8 + c1col]) * f1;
           const float v2 = (acc[2] + red[(ia + 8) * 8 + c0col]) * f0;
           const float v3 = (acc[3] + red[(ia + 8) * 8 + c1col]) * f1;
-          if (a.S == 1) {
+          if (a.S == 1 && a.fuse && i_rb == 0) {
+            gate[0] = v0; gate[1] = v1; gate[2] = v2; gate[3] = v3;   // the gate unit: kept for the up unit
+          } else if (a.S == 1) {
             const int row_a = rb * ROWS + ia, row_b = row_a + 8;
             auto put = [&](int row, int col, float v) {
               if (row < P.n && col < a.batch)
                 P.y[static_cast<int64_t>(col) * P.n + row] =
                     XBF ? __bfloat16_as_ushort(__float2bfloat16_rn(v)) : __half_as_ushort(__float2half_rn(v));
             };
-            put(row_a, c0col, v0);
-            put(row_a, c1col, v1);
-            put(row_b, c0col, v2);
-            put(row_b, c1col, v3);
+            put(row_a, c0col, a.fuse ? silu(gate[0]) * v0 : v0);
+            put(row_a, c1col, a.fuse ? silu(gate[1]) * v1 : v1);
+            put(row_b, c0col, a.fuse ? silu(gate[2]) * v2 : v2);
+            put(row_b, c1col, a.fuse ? silu(gate[3]) * v3 : v3);
           } else {
             red[ia * 8 + c0col] = v0;                              // this CTA's partial, in output units
             red[ia * 8 + c1col] = v1;
@@ -586,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   if (a.S > 1 && ng <= 0) {
     // a grouped launch splits every problem into S chunks; a short problem leaves some empty
     float* red = reinterpret_cast<float*>(sm + L::red);
-    for (int i = threadIdx.x; i < ROWS * 8; i += kThreads) red[i] = 0.f;
+    for (int i = threadIdx.x; i < (a.fuse ? 2 : 1) * ROWS * 8; i += kThreads) red[i] = 0.f;
   }
   if (a.S > 1) {
     // one row block per cluster: the S K-chunks' partial sums meet in distributed shared memory;
@@ -602,6 +617,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         const int row = rb * ROWS + lrow;
         float v = 0.f;
         for (int p = 0; p < a.S; ++p) v += ld_dsmem(red + (lrow * 8 + col) * 4, static_cast<uint32_t>(p));
+        if (a.fuse) {                                              // v is the gate; the up partials follow
+          float u = 0.f;
+          for (int p = 0; p < a.S; ++p)
+            u += ld_dsmem(red + (ROWS * 8 + lrow * 8 + col) * 4, static_cast<uint32_t>(p));
+          v = silu(v) * u;
+        }
         if (row < P.n)
           P.y[static_cast<int64_t>(col) * P.n + row] =
               XBF ? __bfloat16_as_ushort(__float2bfloat16_rn(v)) : __half_as_ushort(__float2half_rn(v));
@@ -842,6 +863,44 @@ lb_status launch_many(const lb_gemv_problem* probs, int count, int batch, cudaSt
   return launch_args<FMT, XBF, BP>(args, best_s, units, smem, st);
 }
 
+// SiLU-gated pair h = silu(W_gate x) * (W_up x): one CTA (S > 1: one cluster of S CTAs) per
+// 128-row block runs the block's gate rows, then its up rows, on one x prologue.  S comes from the
+// same time model, with two units of work per CTA.
+template <int FMT, bool XBF, int BP>
+lb_status launch_pair(const lb_weight& Wg, const lb_weight& Wu, const uint16_t* x, int batch, uint16_t* h,
+                      cudaStream_t st) {
+  using L = Layout<FMT, BP>;
+  const int sms = lb::sm_count();
+  const double t_group = 16384.0 * (FmtTraits<FMT>::gbytes + 2) / 128.0 / 40.0;   // ns per 128x128 tile
+  const int G = static_cast<int>(Wg.k / lb::kGroup);
+  const int units = static_cast<int>((Wg.n + ROWS - 1) / ROWS);
+  auto chunk = [](int g, int S) { return S == 1 ? g : ((g + S - 1) / S + GS - 1) / GS * GS; };
+  int best_s = 0;
+  double best_t = 1e30;
+  for (int s_try = 1; s_try <= kMaxCluster; ++s_try) {
+    const int g = chunk(G, s_try);
+    if (s_try > 1 && (G + g - 1) / g != s_try) continue;            // every rank has groups
+    if (L::total(g) > kSmemMax) continue;
+    const int clusters = max(1, sms / s_try);
+    const int waves = (units + clusters - 1) / clusters;
+    const double t = waves * ((s_try == 1 ? 2500.0 : 3000.0) + 2 * g * t_group);
+    if (t < best_t * 0.999) { best_t = t; best_s = s_try; }
+  }
+  if (best_s == 0) return lb::fail(LB_ERR_UNSUPPORTED, "lb_gemv_swiglu: K = %d too long at batch %d", G * lb::kGroup, batch);
+  Args args;
+  memset(&args, 0, sizeof(args));
+  const int gpc = chunk(G, best_s);
+  lb_status s = fill_prob<FMT>(Wg, x, h, gpc, args.p[0]);
+  if (s != LB_OK) return s;
+  s = fill_prob<FMT>(Wu, x, h, gpc, args.p[1]);
+  if (s != LB_OK) return s;
+  args.count = 2;
+  args.batch = batch;
+  args.S = best_s;
+  args.fuse = 1;
+  return launch_args<FMT, XBF, BP>(args, best_s, units, L::total(gpc), st);
+}
+
 template <int FMT, bool XBF>
 lb_status launch_b(const lb_weight& W, const uint16_t* x, int batch, uint16_t* y, cudaStream_t st) {
   switch (pad_batch(batch)) {
@@ -849,6 +908,16 @@ lb_status launch_b(const lb_weight& W, const uint16_t* x, int batch, uint16_t* y
     case 2: return launch_t<FMT, XBF, 2>(W, x, batch, y, st);
     case 4: return launch_t<FMT, XBF, 4>(W, x, batch, y, st);
     default: return launch_t<FMT, XBF, 8>(W, x, batch, y, st);
+  }
+}
+template <int FMT, bool XBF>
+lb_status launch_pb(const lb_weight& Wg, const lb_weight& Wu, const uint16_t* x, int batch, uint16_t* h,
+                    cudaStream_t st) {
+  switch (pad_batch(batch)) {
+    case 1: return launch_pair<FMT, XBF, 1>(Wg, Wu, x, batch, h, st);
+    case 2: return launch_pair<FMT, XBF, 2>(Wg, Wu, x, batch, h, st);
+    case 4: return launch_pair<FMT, XBF, 4>(Wg, Wu, x, batch, h, st);
+    default: return launch_pair<FMT, XBF, 8>(Wg, Wu, x, batch, h, st);
   }
 }
 template <int FMT, bool XBF>
@@ -885,6 +954,16 @@ lb_status launch_gemv(const lb_weight& W, const void* x, int xdt, int batch, voi
   if (W.fmt == LB_FMT_1BIT_G128)
     return bf ? launch_b<1, true>(W, xs, batch, ys, st) : launch_b<1, false>(W, xs, batch, ys, st);
   return bf ? launch_b<2, true>(W, xs, batch, ys, st) : launch_b<2, false>(W, xs, batch, ys, st);
+}
+
+lb_status launch_gemv_swiglu(const lb_weight& Wg, const lb_weight& Wu, const void* x, int xdt, int batch, void* h,
+                             cudaStream_t st) {
+  const uint16_t* xs = static_cast<const uint16_t*>(x);
+  uint16_t* hs = static_cast<uint16_t*>(h);
+  const bool bf = xdt == LB_BF16;
+  if (Wg.fmt == LB_FMT_1BIT_G128)
+    return bf ? launch_pb<1, true>(Wg, Wu, xs, batch, hs, st) : launch_pb<1, false>(Wg, Wu, xs, batch, hs, st);
+  return bf ? launch_pb<2, true>(Wg, Wu, xs, batch, hs, st) : launch_pb<2, false>(Wg, Wu, xs, batch, hs, st);
 }
 
 lb_status launch_gemv_batched(const lb_gemv_problem* probs, int count, int xdt, int batch, cudaStream_t st) {

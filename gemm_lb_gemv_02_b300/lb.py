@@ -30,7 +30,7 @@ STATUS_NAMES = {0: "LB_OK", 1: "LB_ERR_NULL", 2: "LB_ERR_SHAPE", 3: "LB_ERR_ALIG
 # Symbols declared in include/lb.h (checked by the tests against the header and the library).
 EXPORTED = ("lb_status_string", "lb_last_error", "lb_version", "lb_packed_bytes", "lb_pack_1bit",
             "lb_pack_ternary", "lb_gemv", "lb_gemm_workspace_bytes", "lb_gemm", "lb_device_error",
-            "lb_gemm_noalloc", "lb_gemv_batched", "lb_embed")
+            "lb_gemm_noalloc", "lb_gemv_batched", "lb_embed", "lb_gemv_swiglu")
 LB_GEMM_NOALLOC_SCRATCH_BYTES = 8 << 20
 LB_GEMV_BATCH_MAX = 8
 
@@ -72,6 +72,7 @@ def _load():
         "lb_gemm_noalloc": ([ctypes.POINTER(lb_weight), vp, i32, i64, vp, i32, vp], i32),
         "lb_gemv_batched": ([ctypes.POINTER(lb_gemv_problem), i32, i32, i32, vp], i32),
         "lb_embed": ([ctypes.POINTER(lb_weight), vp, i64, vp, i32, vp], i32),
+        "lb_gemv_swiglu": ([ctypes.POINTER(lb_weight), ctypes.POINTER(lb_weight), vp, i32, i32, vp, vp], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -181,6 +182,12 @@ def lb_gemm(W: lb_weight, x, xdt: int, m: int, y, ydt: int, workspace, workspace
 def lb_gemm_noalloc(W: lb_weight, x, xdt: int, m: int, y, ydt: int, stream=None) -> None:
     """lb_gemm without a workspace: the library stages activations in its own static scratch."""
     _check(_lib.lb_gemm_noalloc(ctypes.byref(W), _ptr(x), xdt, m, _ptr(y), ydt, _stream(stream)), "lb_gemm_noalloc")
+
+
+def lb_gemv_swiglu(Wg: lb_weight, Wu: lb_weight, x, xdt: int, batch: int, h, stream=None) -> None:
+    """h = silu(Wg x) * (Wu x) in one launch."""
+    _check(_lib.lb_gemv_swiglu(ctypes.byref(Wg), ctypes.byref(Wu), _ptr(x), xdt, batch, _ptr(h), _stream(stream)),
+           "lb_gemv_swiglu")
 
 
 def lb_embed(W: lb_weight, ids, count: int, out, out_dtype: int, stream=None) -> None:

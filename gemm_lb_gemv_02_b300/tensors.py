@@ -88,6 +88,16 @@ def gemv_batched(problems, ys=None, stream=None) -> list:
     return ys
 
 
+def gemv_swiglu(Wg: PackedWeight, Wu: PackedWeight, x: torch.Tensor, h: torch.Tensor | None = None,
+                stream=None) -> torch.Tensor:
+    """h[b] = silu(Wg x[b]) * (Wu x[b]) for x [batch][k] (batch 1..8), output in the dtype of x."""
+    assert x.is_cuda and x.is_contiguous() and x.dim() == 2 and x.shape[1] == Wg.k
+    if h is None:
+        h = torch.empty(x.shape[0], Wg.n, dtype=x.dtype, device=x.device)
+    lb.lb_gemv_swiglu(Wg.struct(), Wu.struct(), x, dtype_code(x.dtype), x.shape[0], h, stream)
+    return h
+
+
 def gemm(W: PackedWeight, x: torch.Tensor, out_dtype: torch.dtype = torch.bfloat16,
          y: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Y[m][n] = X W^T for X [m][k]; output dtype out_dtype."""

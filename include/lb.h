@@ -161,6 +161,28 @@ typedef struct lb_gemv_problem {
 lb_status lb_gemv_batched(const lb_gemv_problem* problems, int count, int xdt, int batch, lb_stream stream);
 
 /*
+ * SiLU-gated pair of one decoder layer's feed-forward block in one launch:
+ *     h[b][n] = silu(g[b][n]) * u[b][n],   g = W_gate x[b],  u = W_up x[b],  silu(z) = z / (1 + e^-z),
+ * with g and u each computed exactly as lb_gemv computes them (FP32 accumulation), combined in FP32
+ * and rounded once to `xdt` (RNE); g and u are never stored.  (openclawradar.com, "Bonsai 1.7B
+ * Modelo Ternario Alcanza 442 T/s en M4 Max", section "Detalles técnicos": the fastest decode came
+ * from kernels specialised at the matvec / FFN level; 7minutos.es, "PrismML lanza Bonsai 27B": the
+ * models are builds of a Qwen3-family base, whose feed-forward block is SiLU-gated.)  One CTA
+ * (or cluster) per 128-row block runs the block's gate rows and then its up rows on one prologue of
+ * x, so the pair costs one launch and one x prologue.
+ *
+ * Wg, Wu   : packed matrices of the same format and shape (N x K).
+ * x        : device [batch][K] of `xdt`, 16-byte aligned;  h : device [batch][N] of `xdt`, 16-byte
+ *            aligned, caller-owned, not overlapping x.
+ * batch    : 1 .. 8, with the K limits of lb_gemv.
+ * Asynchronous on `stream`.  Errors (no launch): LB_ERR_NULL, LB_ERR_SHAPE (different shapes,
+ * batch), LB_ERR_ALIGN, LB_ERR_DTYPE, LB_ERR_UNSUPPORTED (different formats, K above the limit),
+ * LB_ERR_CUDA if the launch fails.
+ */
+lb_status lb_gemv_swiglu(const lb_weight* Wg, const lb_weight* Wu, const void* x, int xdt, int batch, void* h,
+                         lb_stream stream);
+
+/*
  * Workspace bytes that lb_gemm needs for an m x k activation matrix of dtype `xdt` against an
  * n x k weight (0 means none is needed).  Pure host arithmetic.
  */

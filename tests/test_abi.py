@@ -113,6 +113,22 @@ def test_embed_validation():
     assert _status(lb.lb_embed, lb.make_weight(2, 64, 200, A16, A16), A16, 3, A16, lb.LB_F16, 0) == "LB_ERR_SHAPE"
 
 
+def test_gemv_swiglu_validation():
+    Wg = lb.make_weight(lb.LB_FMT_TERNARY_G128, 64, 256, A16, A16)
+    Wu = lb.make_weight(lb.LB_FMT_TERNARY_G128, 64, 256, A16, A16)
+    assert _status(lb.lb_gemv_swiglu, Wg, Wu, None, lb.LB_F16, 1, A16, 0) == "LB_ERR_NULL"
+    assert _status(lb.lb_gemv_swiglu, Wg, Wu, A16, lb.LB_F16, 1, None, 0) == "LB_ERR_NULL"
+    assert _status(lb.lb_gemv_swiglu, Wg, Wu, A16, 9, 1, A16, 0) == "LB_ERR_DTYPE"
+    assert _status(lb.lb_gemv_swiglu, Wg, Wu, A16, lb.LB_F16, 0, A16, 0) == "LB_ERR_SHAPE"
+    assert _status(lb.lb_gemv_swiglu, Wg, Wu, A16, lb.LB_F16, 9, A16, 0) == "LB_ERR_SHAPE"
+    assert _status(lb.lb_gemv_swiglu, Wg, Wu, MIS, lb.LB_F16, 1, A16, 0) == "LB_ERR_ALIGN"
+    assert _status(lb.lb_gemv_swiglu, Wg, Wu, A16, lb.LB_F16, 1, MIS, 0) == "LB_ERR_ALIGN"
+    assert _status(lb.lb_gemv_swiglu, Wg, lb.make_weight(2, 48, 256, A16, A16), A16, lb.LB_F16, 1, A16, 0) == "LB_ERR_SHAPE"
+    assert _status(lb.lb_gemv_swiglu, Wg, lb.make_weight(2, 64, 384, A16, A16), A16, lb.LB_F16, 1, A16, 0) == "LB_ERR_SHAPE"
+    assert _status(lb.lb_gemv_swiglu, Wg, lb.make_weight(1, 64, 256, A16, A16), A16, lb.LB_F16, 1, A16, 0) == "LB_ERR_UNSUPPORTED"
+    assert _status(lb.lb_gemv_swiglu, Wg, lb.make_weight(2, 64, 256, None, A16), A16, lb.LB_F16, 1, A16, 0) == "LB_ERR_NULL"
+
+
 def test_gemv_batched_validation():
     W1 = lb.make_weight(lb.LB_FMT_1BIT_G128, 16, 128, A16, A16)
     Wt = lb.make_weight(lb.LB_FMT_TERNARY_G128, 16, 128, A16, A16)
