@@ -47,7 +47,7 @@ LAYERS = 36                      # distinct layer-set copies per step (weights >
 # DRAM bytes per headline GEMV launch from an ncu capture of one layer set (14.62 MB / 4 launches);
 # the algorithmic bytes are 14.55 MB per set, so nothing is re-read.  Set to None when the kernel
 # changes until a new capture is taken.
-GEMV_TRAFFIC_PER_LAUNCH = 3.655e6
+GEMV_TRAFFIC_PER_LAUNCH = 3.662e6
 L2_BYTES = 126 * 2 ** 20
 METRIC = "packed-weight GEMV HBM GB/s (% of peak) at batch 1; prefill GEMM TFLOP/s"
 
@@ -632,7 +632,7 @@ def run_ours(args, ws, rank, local):
         "roofline": {"bound": "hbm", "achieved": round(per_rank_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(per_rank_gbs / peaks["hbm_gbs"], 4), "traffic": GEMV_TRAFFIC_PER_LAUNCH,
                      "traffic_basis": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one layer set "
-                                      "(4 launches) / 4, bytes per launch; kernel as of commit cd6452a "
+                                      "(4 launches) / 4, bytes per launch; kernel as of commit 2b2edaa "
                                       "(summary under profiles/, gemv_kernel on the c2 layer set)",
                      "kernel": "gemv_kernel<ternary, f16 x, batch 1> (4 launches per layer set: "
                                "q/k/v grouped, o, gate/up grouped, down)",

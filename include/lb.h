@@ -26,8 +26,8 @@
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream); work is enqueued on it.
  *   - Errors are returned as lb_status and never abort the process; nothing traps on the GPU.
  *     lb_last_error() returns a thread-local text for the last failing call of this thread.
- *   - lb_gemv / lb_gemm validate their arguments on the host and then launch asynchronously:
- *     LB_OK means "enqueued".  The pack calls synchronise `stream` to read the device-side
+ *   - lb_gemv, lb_gemv_batched, lb_gemv_swiglu, lb_gemm, lb_gemm_noalloc and lb_embed validate
+ *     their arguments on the host and then launch asynchronously: LB_OK means "enqueued".  The pack calls synchronise `stream` to read the device-side
  *     validation result, so their LB_OK means "done and valid".
  *   - Thread safety: every call may be made from any host thread; pack calls serialise on an
  *     internal mutex (they share one device-side validation word per device).
