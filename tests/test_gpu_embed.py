@@ -41,7 +41,7 @@ def _run_guarded(pw, ids, odt):
 
 @pytest.mark.parametrize("fmt", ["1bit", "ternary"])
 @pytest.mark.parametrize("odt", ["f16", "bf16"])
-@pytest.mark.parametrize("n,k,count", [(1, 128, 1), (37, 384, 5), (300, 2048, 333), (1000, 640, 64)])
+@pytest.mark.parametrize("n,k,count", [(1, 128, 1), (37, 384, 5), (300, 2048, 333), (1000, 640, 64), (9, 17536, 40)])
 def test_embed_shapes(fmt, odt, n, k, count):
     pw, codes, scales = _packed(fmt, n, k, seed=n + k)
     g = torch.Generator().manual_seed(count + n)

@@ -114,3 +114,22 @@ def test_gemm_1bit_block_prefill_sampled():
     rows = np.unique(np.concatenate([[0, 255, 256, 511], rng.integers(0, 512, 60)]))
     cols = np.unique(np.concatenate([np.arange(8), np.arange(mat.n - 8, mat.n), rng.integers(0, mat.n, 600)]))
     _check(pw, codes, scales, x, torch.bfloat16, "1-bit block prefill", rows=rows, cols=cols)
+
+
+@pytest.mark.parametrize("fmt", ["1bit", "ternary"])
+def test_gemm_many_token_tiles(fmt):
+    """4096 tokens (16 token tiles of 256) with a ragged row count; every output checked."""
+    m, n, k = 4096, 400, 1024
+    pw, codes, scales = _packed(fmt, n, k, seed=90)
+    x = synth.activations(m, k, "bf16", seed=91)
+    _check(pw, codes, scales, x, torch.bfloat16, f"gemm {fmt} m={m}")
+
+
+@pytest.mark.parametrize("fmt", ["1bit", "ternary"])
+def test_gemm_long_k(fmt):
+    """K = 17536 (137 groups: the scale rows are not a multiple of 16 bytes, so the scales take
+    the non-TMA path, and 274 pipeline stages), 300 tokens."""
+    m, n, k = 300, 256, 17536
+    pw, codes, scales = _packed(fmt, n, k, seed=92)
+    x = synth.activations(m, k, "bf16", seed=93)
+    _check(pw, codes, scales, x, torch.bfloat16, f"gemm {fmt} k={k}")

@@ -187,3 +187,16 @@ def test_gemv_batched_k_split_with_empty_chunks(fmt, batch):
     for (pw, codes, scales), (n, k), x, y in zip(packed, shapes, xs, ys):
         y_ref, a = oracle_products(fmt, codes, scales, k, x.cpu())
         check_products(y, y_ref, a, f"batched split {fmt} n={n} k={k} batch={batch}")
+
+
+@pytest.mark.parametrize("fmt", ["1bit", "ternary"])
+@pytest.mark.parametrize("batch,k", [(1, 352256), (2, 196608), (4, 98304), (8, 49152)])
+def test_gemv_at_k_limit(fmt, batch, k):
+    """Each batch class at the largest K lb_gemv accepts (the K split then uses the widest
+    cluster), with a ragged row count."""
+    n = 20
+    pw, codes, scales = _packed(fmt, n, k, seed=k + batch)
+    x = synth.activations(batch, k, "bf16", seed=batch).cuda()
+    y = _run_guarded(pw, x)
+    y_ref, a = oracle_products(fmt, codes, scales, k, x.cpu())
+    check_products(y, y_ref, a, f"{fmt} k-limit batch={batch} k={k}")

@@ -63,7 +63,7 @@ def _run_guarded(pg, pu, x):
 
 @pytest.mark.parametrize("fmt", ["1bit", "ternary"])
 @pytest.mark.parametrize("xdt", ["f16", "bf16"])
-@pytest.mark.parametrize("n,k", [(16, 128), (100, 384), (333, 1024), (64, 8192), (6144, 2048)])
+@pytest.mark.parametrize("n,k", [(16, 128), (100, 384), (333, 1024), (64, 8192), (6144, 2048), (20, 49152)])
 def test_swiglu_shapes(fmt, xdt, n, k):
     """Ragged row counts, one and many groups, a long K with few rows (split across a cluster),
     and the 1.7B-class gate/up shape."""
