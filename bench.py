@@ -387,6 +387,29 @@ def measure_gemm_row(lbt, peaks, sel=None):
     return rows
 
 
+def measure_copy_reference(peaks, sel=None):
+    """Context for the GEMV rows: a plain device-to-device copy (cudaMemcpyAsync through torch) of
+    44 MB, the LM-head GEMV's byte count, rotated over buffers larger than L2.  The measured peak
+    comes from a 4 GB copy; one launch of this size pays its ramp-up and tail."""
+    name = "ref_copy_44MB"
+    if not _want(name, sel):
+        return {}
+    nb = 44 * 1000 * 1000
+    copies = _copies_for(2 * nb)
+    src = [torch.empty(nb, dtype=torch.uint8, device="cuda") for _ in range(copies)]
+    dst = [torch.empty(nb, dtype=torch.uint8, device="cuda") for _ in range(copies)]
+    steps = copies * 2
+    g = _graph(lambda: [dst[i % copies].copy_(src[i % copies]) for i in range(steps)])
+    _time_graph(g)
+    ms = _time_graph(g, reps=3) / steps
+    gbs = 2 * nb / (ms * 1e-3) / 1e9
+    del src, dst, g
+    torch.cuda.empty_cache()
+    return {name: {"bytes_read_plus_written": 2 * nb, "us_per_copy": round(ms * 1e3, 2), "GB_s": round(gbs, 1),
+                   "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 3),
+                   "note": "library copy, not this library's kernel: the bandwidth one launch of this size reaches"}}
+
+
 SWIGLU_ROWS = (  # row name, workload, batch
     ("swiglu_c2_b1", "c2", 1),
     ("swiglu_c4t_b1", "c4t", 1),
@@ -633,6 +656,7 @@ def run_ours(args, ws, rank, local):
         rows.update(measure_gemm_row(lbt, peaks, sel))
         rows.update(measure_embed_rows(lbt, peaks, sel))
         rows.update(measure_swiglu_rows(lbt, peaks, sel))
+        rows.update(measure_copy_reference(peaks, sel))
     assert lbl.lb_device_error(clear=True) == 0, "device error word set"
 
     if rank != 0:
