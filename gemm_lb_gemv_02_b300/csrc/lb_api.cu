@@ -86,6 +86,11 @@ lb_status check_weight(const lb_weight* W) {
 
 bool valid_dtype(int d) { return d == LB_F16 || d == LB_BF16; }
 
+// Launch-shape limits of the GEMM: 65535 token tiles of 256 along grid y; the activation prologue
+// runs one thread per 16 activations, at most 2^31 - 1 blocks of 256 threads.
+constexpr int64_t kGemmMaxM = int64_t(65535) * 256;
+constexpr int64_t kGemmMaxMK = (int64_t(1) << 31) * 4096 - 4096;
+
 }  // namespace
 
 extern "C" {
@@ -213,7 +218,9 @@ lb_status lb_gemm(const lb_weight* W, const void* x, int xdt, int64_t m, void* y
   if (s != LB_OK) return s;
   if (!x || !y) return fail(LB_ERR_NULL, "x and y must be non-NULL");
   if (!valid_dtype(xdt) || !valid_dtype(ydt)) return fail(LB_ERR_DTYPE, "unknown dtype (x %d, y %d)", xdt, ydt);
-  if (m < 1 || m > (int64_t(1) << 24)) return fail(LB_ERR_SHAPE, "m must be in [1, 2^24] (got %lld)", (long long)m);
+  if (m < 1 || m > kGemmMaxM) return fail(LB_ERR_SHAPE, "m must be in [1, %lld] (got %lld)", (long long)kGemmMaxM, (long long)m);
+  if ((m + 127) / 128 * 128 * W->k > kGemmMaxMK)
+    return fail(LB_ERR_SHAPE, "m x k too large for one call (m %lld, k %lld)", (long long)m, (long long)W->k);
   if (W->n % 16) return fail(LB_ERR_SHAPE, "lb_gemm needs n %% 16 == 0 (got %lld)", (long long)W->n);
   if (!lb::aligned16(x) || !lb::aligned16(y)) return fail(LB_ERR_ALIGN, "x and y must be 16-byte aligned");
   const size_t need = lb::gemm_workspace_bytes(m, W->k);
@@ -230,7 +237,9 @@ lb_status lb_gemm_noalloc(const lb_weight* W, const void* x, int xdt, int64_t m,
   if (s != LB_OK) return s;
   if (!x || !y) return fail(LB_ERR_NULL, "x and y must be non-NULL");
   if (!valid_dtype(xdt) || !valid_dtype(ydt)) return fail(LB_ERR_DTYPE, "unknown dtype (x %d, y %d)", xdt, ydt);
-  if (m < 1 || m > (int64_t(1) << 24)) return fail(LB_ERR_SHAPE, "m must be in [1, 2^24] (got %lld)", (long long)m);
+  if (m < 1 || m > kGemmMaxM) return fail(LB_ERR_SHAPE, "m must be in [1, %lld] (got %lld)", (long long)kGemmMaxM, (long long)m);
+  if ((m + 127) / 128 * 128 * W->k > kGemmMaxMK)
+    return fail(LB_ERR_SHAPE, "m x k too large for one call (m %lld, k %lld)", (long long)m, (long long)W->k);
   if (W->n % 16) return fail(LB_ERR_SHAPE, "lb_gemm_noalloc needs n %% 16 == 0 (got %lld)", (long long)W->n);
   if (!lb::aligned16(x) || !lb::aligned16(y)) return fail(LB_ERR_ALIGN, "x and y must be 16-byte aligned");
   return lb::launch_gemm_noalloc(*W, x, xdt, m, y, ydt, reinterpret_cast<cudaStream_t>(stream));
@@ -241,7 +250,7 @@ lb_status lb_embed(const lb_weight* W, const int32_t* ids, int64_t count, void* 
   lb_status s = check_weight(W);
   if (s != LB_OK) return s;
   if (count < 0 || count > INT32_MAX) return fail(LB_ERR_SHAPE, "count must be in [0, 2^31) (got %lld)", (long long)count);
-  if (count * ((W->k + 1023) / 1024) > (int64_t(1) << 34))
+  if (count * ((W->k + 1023) / 1024) > (int64_t(1) << 34) - 8)
     return fail(LB_ERR_SHAPE, "count x K too large for one launch (count %lld, k %lld)", (long long)count,
                 (long long)W->k);
   if (!valid_dtype(out_dtype)) return fail(LB_ERR_DTYPE, "unknown output dtype %d", out_dtype);

@@ -830,6 +830,8 @@ lb_status launch_many(const lb_gemv_problem* probs, int count, int batch, cudaSt
     units += static_cast<int>((probs[i].W.n + ROWS - 1) / ROWS);
     gmax = max(gmax, static_cast<int>(probs[i].W.k / lb::kGroup));
   }
+  if (units > 65535)
+    return lb::fail(LB_ERR_SHAPE, "lb_gemv_batched: %d row blocks of 128 exceed one launch (65535)", units);
   auto chunk = [](int G, int S) { return S == 1 ? G : ((G + S - 1) / S + GS - 1) / GS * GS; };
   int best_s = 0;
   double best_t = 1e30;
@@ -887,6 +889,7 @@ lb_status launch_pair(const lb_weight& Wg, const lb_weight& Wu, const uint16_t* 
     if (t < best_t * 0.999) { best_t = t; best_s = s_try; }
   }
   if (best_s == 0) return lb::fail(LB_ERR_UNSUPPORTED, "lb_gemv_swiglu: K = %d too long at batch %d", G * lb::kGroup, batch);
+  if (units > 65535) return lb::fail(LB_ERR_SHAPE, "lb_gemv_swiglu: %d row blocks of 128 exceed one launch (65535)", units);
   Args args;
   memset(&args, 0, sizeof(args));
   const int gpc = chunk(G, best_s);

@@ -156,7 +156,8 @@ typedef struct lb_gemv_problem {
  * xdt      : LB_F16 or LB_BF16 for every x and y;  batch : 1 .. 8 for every problem.
  * No y may overlap another problem's x or y.  Asynchronous on `stream`.  Errors (no launch):
  * LB_ERR_NULL, LB_ERR_SHAPE (count or batch out of range, a bad n / k), LB_ERR_ALIGN, LB_ERR_DTYPE,
- * LB_ERR_UNSUPPORTED (mixed formats, or a k above the lb_gemv limit), LB_ERR_CUDA if the launch fails.
+ * LB_ERR_UNSUPPORTED (mixed formats, or a k above the lb_gemv limit), LB_ERR_SHAPE also when the
+ * problems hold more than 65535 blocks of 128 rows in total, LB_ERR_CUDA if the launch fails.
  */
 lb_status lb_gemv_batched(const lb_gemv_problem* problems, int count, int xdt, int batch, lb_stream stream);
 
@@ -174,7 +175,7 @@ lb_status lb_gemv_batched(const lb_gemv_problem* problems, int count, int xdt, i
  * Wg, Wu   : packed matrices of the same format and shape (N x K).
  * x        : device [batch][K] of `xdt`, 16-byte aligned;  h : device [batch][N] of `xdt`, 16-byte
  *            aligned, caller-owned, not overlapping x.
- * batch    : 1 .. 8, with the K limits of lb_gemv.
+ * batch    : 1 .. 8, with the K limits of lb_gemv;  N <= 65535 * 128.
  * Asynchronous on `stream`.  Errors (no launch): LB_ERR_NULL, LB_ERR_SHAPE (different shapes,
  * batch), LB_ERR_ALIGN, LB_ERR_DTYPE, LB_ERR_UNSUPPORTED (different formats, K above the limit),
  * LB_ERR_CUDA if the launch fails.
@@ -202,9 +203,11 @@ lb_status lb_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, int xdt, size
  * workspace        : device scratch of at least lb_gemm_workspace_bytes(...) bytes, 256-byte
  *                    aligned, used only during this call's kernels (may be reused afterwards).
  * Asynchronous on `stream`.  Errors (no launch): LB_ERR_NULL, LB_ERR_SHAPE, LB_ERR_ALIGN,
- * LB_ERR_DTYPE, LB_ERR_WORKSPACE; LB_ERR_CUDA.  Any m is served by the same kernels: a token tile
- * holding fewer than 256 tokens runs its tensor-core products only as wide as its token count
- * (rounded up to 16), so mid-size m (16 .. 128) pays for the tokens it has.
+ * LB_ERR_DTYPE, LB_ERR_WORKSPACE; LB_ERR_CUDA.  Limits of one call: 1 <= m <= 65535 * 256 and
+ * ceil(m / 128) * 128 * k <= (2^31 - 1) * 4096 (LB_ERR_SHAPE beyond).  Any m is served by the
+ * same kernels: a token tile holding fewer than 256 tokens runs its tensor-core products only as
+ * wide as its token count (rounded up to 16), so mid-size m (16 .. 128) pays for the tokens it
+ * has.
  */
 lb_status lb_gemm(const lb_weight* W, const void* x, int xdt, int64_t m, void* y, int ydt,
                   void* workspace, size_t workspace_bytes, lb_stream stream);
@@ -221,7 +224,7 @@ lb_status lb_gemm(const lb_weight* W, const void* x, int xdt, int64_t m, void* y
  * ids       : device int32 [count] row ids, 4-byte aligned.  An id outside [0, N) is not a
  *             table row: its output row is written as +0 and bit 2 of the device error word is
  *             set (lb_device_error); the call itself cannot see device data and returns LB_OK.
- * count     : 0 .. 2^31 - 1 rows with count * ceil(K / 1024) <= 2^34; 0 launches nothing (ids
+ * count     : 0 .. 2^31 - 1 rows with count * ceil(K / 1024) <= 2^34 - 8; 0 launches nothing (ids
  *             and out may then be NULL).
  * out       : device [count][K] of `out_dtype`, 16-byte aligned, caller-owned.
  * Asynchronous on `stream`.  Errors (no launch): LB_ERR_NULL, LB_ERR_SHAPE, LB_ERR_ALIGN,

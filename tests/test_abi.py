@@ -95,6 +95,12 @@ def test_gemm_validation():
     assert _status(lb.lb_gemm, lb.make_weight(1, 250, 256, A16, A16), A16, lb.LB_BF16, 5, A16, lb.LB_BF16,
                    A16, need, 0) == "LB_ERR_SHAPE"
     assert _status(lb.lb_gemm, W, A16, 5, 5, A16, lb.LB_BF16, A16, need, 0) == "LB_ERR_DTYPE"
+    # launch-shape limits: 65535 token tiles of 256; the activation prologue's grid
+    W128 = lb.make_weight(lb.LB_FMT_TERNARY_G128, 256, 128, A16, A16)
+    assert _status(lb.lb_gemm, W128, A16, lb.LB_BF16, 65535 * 256 + 1, A16, lb.LB_BF16, A16, need, 0) == "LB_ERR_SHAPE"
+    assert _status(lb.lb_gemm, W128, A16, lb.LB_BF16, 65535 * 256, A16, lb.LB_BF16, A16, need, 0) == "LB_ERR_WORKSPACE"
+    Wk = lb.make_weight(lb.LB_FMT_TERNARY_G128, 256, 1 << 24, A16, A16)
+    assert _status(lb.lb_gemm, Wk, A16, lb.LB_BF16, 1 << 20, A16, lb.LB_BF16, A16, need, 0) == "LB_ERR_SHAPE"
 
 
 def test_embed_validation():
@@ -127,6 +133,13 @@ def test_gemv_swiglu_validation():
     assert _status(lb.lb_gemv_swiglu, Wg, lb.make_weight(2, 64, 384, A16, A16), A16, lb.LB_F16, 1, A16, 0) == "LB_ERR_SHAPE"
     assert _status(lb.lb_gemv_swiglu, Wg, lb.make_weight(1, 64, 256, A16, A16), A16, lb.LB_F16, 1, A16, 0) == "LB_ERR_UNSUPPORTED"
     assert _status(lb.lb_gemv_swiglu, Wg, lb.make_weight(2, 64, 256, None, A16), A16, lb.LB_F16, 1, A16, 0) == "LB_ERR_NULL"
+
+
+def test_grouped_launch_row_block_limit():
+    """More than 65535 blocks of 128 rows cannot be one grouped launch: a clean error, no launch."""
+    big = lb.make_weight(lb.LB_FMT_1BIT_G128, 65536 * 128, 128, A16, A16)
+    assert _status(lb.lb_gemv_batched, [(big, A16, A16)], lb.LB_F16, 1) == "LB_ERR_SHAPE"
+    assert _status(lb.lb_gemv_swiglu, big, big, A16, lb.LB_F16, 1, A16, 0) == "LB_ERR_SHAPE"
 
 
 def test_gemv_batched_validation():
