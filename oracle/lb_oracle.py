@@ -44,6 +44,8 @@ import numpy as np
 GROUP = 128          # [P1] box: "cada 128 pesos comparten un factor de escala FP16"
 FMT_1BIT = 1
 FMT_TERNARY = 2
+FMT_TERNARY5 = 3     # ternary codes stored 5 per byte (base 3), 26 bytes per 128-weight group
+T5_GROUP_BYTES = 26  # 25 bytes of 5 digits + 1 byte of 3 digits
 TOL_REL = 2e-3
 TOL_ABS = 1e-5
 
@@ -177,6 +179,8 @@ def packed_bytes(fmt: int, n: int, k: int) -> tuple[int, int]:
         return n * k // 8, groups * 2
     if fmt == FMT_TERNARY:
         return n * k // 4, groups * 2
+    if fmt == FMT_TERNARY5:
+        return groups * T5_GROUP_BYTES, groups * 2
     raise OracleError("format", f"unknown format {fmt}")
 
 
@@ -239,6 +243,32 @@ def pack_ternary(t, s) -> tuple[np.ndarray, np.ndarray]:
     return codes, s.copy()
 
 
+def pack_ternary5(t, s) -> tuple[np.ndarray, np.ndarray]:
+    """Ternary codes stored five to a byte ([P4] es.news.hada.io topic 31450, comments: five
+    three-state values fit one byte, 1.6 bits each; [P3] "Arquitectura del Sistema": 1.76
+    effective bits per weight).  Reading used here: digit f = t + 1 in {0, 1, 2}; within each
+    128-weight group, byte j holds weights 5j .. 5j+4 as sum_i f_(5j+i) 3^i (first weight in the
+    lowest digit); byte 25 holds weights 125..127 (its two upper digits are 0).  26 bytes per
+    group, row-major [N][26 K/128]; scales unchanged.
+    """
+    t = np.asarray(t)
+    s = np.asarray(s, dtype=np.uint16)
+    if t.ndim != 2:
+        raise OracleError("shape", "t must be 2-D")
+    n, k = t.shape
+    _check_shape(n, k)
+    if s.shape != (n, k // GROUP):
+        raise OracleError("shape", f"scales must be {(n, k // GROUP)}, got {s.shape}")
+    if not np.all((t == -1) | (t == 0) | (t == 1)):
+        raise OracleError("code", "ternary codes must be -1, 0 or +1")
+    g = k // GROUP
+    f = np.zeros((n, g, 5 * T5_GROUP_BYTES), dtype=np.int64)
+    f[:, :, :GROUP] = t.astype(np.int64).reshape(n, g, GROUP) + 1
+    f = f.reshape(n, g, T5_GROUP_BYTES, 5)
+    codes = sum(f[..., i] * 3 ** i for i in range(5)).astype(np.uint8)
+    return codes.reshape(n, g * T5_GROUP_BYTES), s.copy()
+
+
 # ---------------------------------------------------------------------------------------
 # Unpacking and dequantisation: w_hat = s_g * t_i ([P2] "Cómo funciona la compresión").
 # ---------------------------------------------------------------------------------------
@@ -260,12 +290,26 @@ def unpack_ternary(codes, k: int) -> np.ndarray:
     return (f - 1).astype(np.int8)
 
 
+def unpack_ternary5(codes, k: int) -> np.ndarray:
+    """codes uint8 [N][26 K/128] (five base-3 digits per byte) -> t int8 [N][K]; a byte above
+    242, or a last byte of a group with a non-zero upper digit, is rejected."""
+    codes = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    n, g = codes.shape[0], k // GROUP
+    b = codes.reshape(n, g, T5_GROUP_BYTES)
+    if np.any(b > 242) or np.any(b[:, :, -1] >= 27):
+        raise OracleError("code", "not a base-3 code byte of this layout")
+    digits = np.stack([(b // 3 ** i) % 3 for i in range(5)], axis=3).reshape(n, g, 5 * T5_GROUP_BYTES)
+    return (digits[:, :, :GROUP] - 1).reshape(n, k).astype(np.int8)
+
+
 def dequantize(fmt: int, codes, scales, k: int) -> np.ndarray:
     """Packed weights -> dense float64 [N][K] with w_hat[n][k] = s[n][k // 128] * t[n][k]."""
     if fmt == FMT_1BIT:
         t = unpack_1bit(codes, k)
     elif fmt == FMT_TERNARY:
         t = unpack_ternary(codes, k)
+    elif fmt == FMT_TERNARY5:
+        t = unpack_ternary5(codes, k)
     else:
         raise OracleError("format", f"unknown format {fmt}")
     s = f16_bits_to_f64(np.asarray(scales, dtype=np.uint16))

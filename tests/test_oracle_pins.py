@@ -126,6 +126,48 @@ def pin_embed():
     assert (out[0, 128:256][t[7, 128:256] == 0] == 0x8000).all()
 
 
+def pin_ternary5():
+    """Five-digit base-3 storage: hand-computed bytes, exact round trip, the printed sizes, and
+    the same products as the 2-bit storage of the same codes."""
+    g = _load("sizes.json")
+    # sizes: 26 bytes of codes + 2 of scale per 128 weights = 1.75 bpw; the page's "five
+    # three-state values in a byte" is 8 / 5 bits, and 1.75 lies between the printed 1.71 and 1.76
+    c, sc = orc.packed_bytes(orc.FMT_TERNARY5, 1, orc.GROUP)
+    assert (c, sc) == (26, 2) and orc.bits_per_weight(orc.FMT_TERNARY5) == 1.75
+    assert 8 / 5 == g["p4_five_trits_per_byte_bits"]["value"]
+    assert g["p2_ternary_info_bpw"]["value"] <= 1.75 <= g["p3_ternary_effective_bpw"]["value"]
+    # hand-computed bytes (digit f = t + 1, first weight of a byte in the lowest digit)
+    one = np.ones((1, 128), dtype=np.int8)
+    s1 = np.full((1, 1), 0x3C00, dtype=np.uint16)
+    c, _ = orc.pack_ternary5(one, s1)                              # f = 2 everywhere
+    assert c[0, :25].tolist() == [242] * 25 and c[0, 25] == 2 + 6 + 18
+    c, _ = orc.pack_ternary5(-one, s1)                             # f = 0
+    assert not c.any()
+    t = np.zeros((1, 128), dtype=np.int8)
+    c, _ = orc.pack_ternary5(t, s1)                                # f = 1: 1 + 3 + 9 + 27 + 81
+    assert c[0, :25].tolist() == [121] * 25 and c[0, 25] == 13
+    t[0, 7] = 1                                                    # byte 1, digit 2: + 3^2
+    t[0, 126] = -1                                                 # byte 25, digit 1: - 3
+    c, _ = orc.pack_ternary5(t, s1)
+    assert c[0, 1] == 130 and c[0, 25] == 10 and c[0, 0] == 121
+    # round trip and equal products with the 2-bit storage
+    rng = np.random.default_rng(11)
+    n, k = 13, 640
+    t = rng.integers(-1, 2, (n, k)).astype(np.int8)
+    sb = (np.abs(rng.standard_normal((n, k // 128))) * 0.03).astype(np.float16).view(np.uint16)
+    c5, s5 = orc.pack_ternary5(t, sb)
+    assert c5.shape == (n, 26 * (k // 128)) and np.array_equal(orc.unpack_ternary5(c5, k), t)
+    c2, s2 = orc.pack_ternary(t, sb)
+    x = rng.standard_normal((3, k))
+    y5, a5 = orc.matvec(orc.FMT_TERNARY5, c5, s5, k, x)
+    y2, a2 = orc.matvec(orc.FMT_TERNARY, c2, s2, k, x)
+    assert np.array_equal(y5, y2) and np.array_equal(a5, a2)
+    bad = c5.copy()
+    bad[0, 25] = 27                                                # a digit past weight 127
+    with pytest.raises(orc.OracleError):
+        orc.unpack_ternary5(bad, k)
+
+
 def pin_silu():
     """silu against 50-digit mpmath, its limits, and the slope constant of the SwiGLU bound."""
     import mpmath
@@ -442,7 +484,7 @@ def pin_tolerance_rule():
 
 
 ALL_PINS = [pin_f16_decode_exhaustive, pin_bf16_decode_exhaustive, pin_f16_encode, pin_bf16_encode, pin_embed,
-            pin_silu, pin_swiglu,
+            pin_silu, pin_swiglu, pin_ternary5,
             pin_sizes,
             pin_demo_group, pin_layout_fixtures, pin_roundtrip_1bit, pin_roundtrip_ternary,
             pin_rowsum_invariant, pin_unit_vectors, pin_bruteforce_exact,
@@ -560,7 +602,22 @@ def _mut_swiglu_swap(monkeypatch):
     monkeypatch.setattr(orc, "swiglu", bad)
 
 
-MUTATIONS = [_mut_silu_sign, _mut_swiglu_swap, _mut_bitorder_big, _mut_sign_strict, _mut_scale_mean, _mut_ternary_field,
+def _mut_t5_digit_order(monkeypatch):
+    real = orc.pack_ternary5
+
+    def bad(t, s):
+        t = np.asarray(t)
+        n, k = t.shape
+        g = k // 128
+        f = np.zeros((n, g, 130), dtype=np.int64)
+        f[:, :, :128] = t.astype(np.int64).reshape(n, g, 128) + 1
+        f = f.reshape(n, g, 26, 5)
+        codes = sum(f[..., i] * 3 ** (4 - i) for i in range(5)).astype(np.uint8)   # first weight highest
+        return codes.reshape(n, g * 26), np.asarray(s, dtype=np.uint16).copy()
+    monkeypatch.setattr(orc, "pack_ternary5", bad)
+
+
+MUTATIONS = [_mut_t5_digit_order, _mut_silu_sign, _mut_swiglu_swap, _mut_bitorder_big, _mut_sign_strict, _mut_scale_mean, _mut_ternary_field,
              _mut_drop_scale, _mut_scale_axis, _mut_f16_bias, _mut_abs_sum, _mut_rne_truncate,
              _mut_bf16_truncate, _mut_embed_row_offset]
 
