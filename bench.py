@@ -140,13 +140,16 @@ def _copies_for(bytes_per_copy: int, minimum: int = 2) -> int:
     return max(minimum, -(-4 * L2_BYTES // max(1, bytes_per_copy)))
 
 
-def _pack_workload(wl, lbt):
-    """Pack every matrix of a workload on the device (via the library's packers)."""
+def _pack_workload(wl, lbt, storage=None):
+    """Pack every matrix of a workload on the device (via the library's packers); storage
+    "ternary5" stores a ternary workload's codes five per byte."""
     packed = []
     for i in range(len(wl.matrices)):
         inp = synth.matrix_inputs(wl, i)
         if wl.fmt == "1bit":
             packed.append(lbt.pack_1bit(inp["w"].cuda()))
+        elif storage == "ternary5":
+            packed.append(lbt.pack_ternary5(inp["t"].cuda(), inp["s"].cuda()))
         else:
             packed.append(lbt.pack_ternary(inp["t"].cuda(), inp["s"].cuda()))
     torch.cuda.synchronize()
@@ -220,9 +223,9 @@ class GemvSet:
     """Rotating copies of a workload's matrices; one 'step' runs every matrix of one copy, issued as
     the grouping says (matrices of one launch share the first one's activations)."""
 
-    def __init__(self, wl, batch, lbt, copies=None, layers_per_step=None, grouping="separate"):
+    def __init__(self, wl, batch, lbt, copies=None, layers_per_step=None, grouping="separate", storage=None):
         self.wl, self.batch, self.lbt = wl, batch, lbt
-        base = _pack_workload(wl, lbt)
+        base = _pack_workload(wl, lbt, storage)
         per_copy = sum(_gemv_bytes(pw, batch) for pw in base)
         self.copies = copies or _copies_for(per_copy)
         self.sets = [base] + [[_clone(pw) for pw in base] for _ in range(self.copies - 1)]
@@ -265,7 +268,7 @@ def _want(name, sel):
     return sel is None or any(name.startswith(p) for p in sel)
 
 
-GEMV_ROWS = (  # row name, workload, batch, grouping
+GEMV_ROWS = (  # row name, workload, batch, grouping[, storage]
     ("gemv_c1_b1", "c1", 1, "separate"),
     ("gemv_c2_b1_7launches", "c2", 1, "separate"),
     ("gemv_c2_b1_1launch", "c2", 1, "one"),
@@ -276,23 +279,27 @@ GEMV_ROWS = (  # row name, workload, batch, grouping
     ("gemv_c4b_b1", "c4b", 1, "layer"),
     ("gemv_c4b_b5", "c4b", 5, "layer"),
     ("gemv_c4t_b1_5launches", "c4t", 1, "separate"),
+    ("gemv_c2_b1_ternary5_7launches", "c2", 1, "separate", "ternary5"),
+    ("gemv_c4t_b1_ternary5_5launches", "c4t", 1, "separate", "ternary5"),
+    ("gemv_c4t_b5_ternary5_5launches", "c4t", 5, "separate", "ternary5"),
 )
 
 
 def measure_gemv_rows(lbt, peaks, sel=None):
     rows = {}
-    for name, key, b, grouping in GEMV_ROWS:
+    for name, key, b, grouping, *storage in GEMV_ROWS:
         wl = synth.WORKLOADS[key]
         if not _want(name, sel):
             continue
-        gs = GemvSet(wl, b, lbt, grouping=grouping)
+        st = storage[0] if storage else None
+        gs = GemvSet(wl, b, lbt, grouping=grouping, storage=st)
         steps = gs.copies * 2
         g = _graph(lambda: [gs.step() for _ in range(steps)])
         _time_graph(g)
         ms = _time_graph(g, reps=3) / steps
         gbs = gs.bytes_per_step / (ms * 1e-3) / 1e9
         rows[name] = {
-            "shape": [[m.n, m.k] for m in wl.matrices], "fmt": wl.fmt, "x": wl.xdtype, "batch": b,
+            "shape": [[m.n, m.k] for m in wl.matrices], "fmt": st or wl.fmt, "x": wl.xdtype, "batch": b,
             "launches": [[wl.matrices[i].name for i in grp] for grp in gs.groups],
             "us_per_layer_set": round(ms * 1e3, 3), "GB_s": round(gbs, 1),
             "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 3),

@@ -74,7 +74,7 @@ lb_status check_shape(int64_t n, int64_t k) {
 
 lb_status check_weight(const lb_weight* W) {
   if (!W) return fail(LB_ERR_NULL, "W is NULL");
-  if (W->fmt != LB_FMT_1BIT_G128 && W->fmt != LB_FMT_TERNARY_G128)
+  if (W->fmt != LB_FMT_1BIT_G128 && W->fmt != LB_FMT_TERNARY_G128 && W->fmt != LB_FMT_TERNARY5_G128)
     return fail(LB_ERR_DTYPE, "unknown weight format %d", (int)W->fmt);
   lb_status s = check_shape(W->n, W->k);
   if (s != LB_OK) return s;
@@ -118,10 +118,14 @@ int lb_version(void) { return 100; }
 
 lb_status lb_packed_bytes(int fmt, int64_t n, int64_t k, size_t* codes_bytes, size_t* scales_bytes) {
   if (!codes_bytes || !scales_bytes) return fail(LB_ERR_NULL, "output pointer is NULL");
-  if (fmt != LB_FMT_1BIT_G128 && fmt != LB_FMT_TERNARY_G128) return fail(LB_ERR_DTYPE, "unknown format %d", fmt);
+  if (fmt != LB_FMT_1BIT_G128 && fmt != LB_FMT_TERNARY_G128 && fmt != LB_FMT_TERNARY5_G128)
+    return fail(LB_ERR_DTYPE, "unknown format %d", fmt);
   lb_status s = check_shape(n, k);
   if (s != LB_OK) return s;
-  *codes_bytes = static_cast<size_t>(n) * static_cast<size_t>(k) / (fmt == LB_FMT_1BIT_G128 ? 8 : 4);
+  if (fmt == LB_FMT_TERNARY5_G128)
+    *codes_bytes = static_cast<size_t>(n) * static_cast<size_t>(k / lb::kGroup) * 26;
+  else
+    *codes_bytes = static_cast<size_t>(n) * static_cast<size_t>(k) / (fmt == LB_FMT_1BIT_G128 ? 8 : 4);
   *scales_bytes = static_cast<size_t>(n) * static_cast<size_t>(k / lb::kGroup) * 2;
   return LB_OK;
 }
@@ -157,6 +161,21 @@ lb_status lb_pack_ternary(const int8_t* t, const uint16_t* s_in, int64_t n, int6
   return LB_OK;
 }
 
+lb_status lb_pack_ternary5(const int8_t* t, const uint16_t* s_in, int64_t n, int64_t k, uint8_t* codes,
+                           uint16_t* scales, lb_stream stream) {
+  lb_status s = check_shape(n, k);
+  if (s != LB_OK) return s;
+  if (!t || !s_in || !codes || !scales) return fail(LB_ERR_NULL, "t, s_in, codes and scales must be non-NULL");
+  if (!lb::aligned16(t) || !lb::aligned16(s_in) || !lb::aligned16(codes) || !lb::aligned16(scales))
+    return fail(LB_ERR_ALIGN, "t, s_in, codes and scales must be 16-byte aligned");
+  std::lock_guard<std::mutex> lk(g_pack_mutex);
+  uint32_t flags = 0;
+  s = lb::launch_pack_ternary5(t, s_in, n, k, codes, scales, reinterpret_cast<cudaStream_t>(stream), &flags);
+  if (s != LB_OK) return s;
+  if (flags & lb::kPackCode) return fail(LB_ERR_CODE, "a ternary code is outside {-1, 0, +1}");
+  return LB_OK;
+}
+
 lb_status lb_gemv(const lb_weight* W, const void* x, int xdt, int batch, void* y, lb_stream stream) {
   lb_status s = check_weight(W);
   if (s != LB_OK) return s;
@@ -164,6 +183,8 @@ lb_status lb_gemv(const lb_weight* W, const void* x, int xdt, int batch, void* y
   if (!valid_dtype(xdt)) return fail(LB_ERR_DTYPE, "unknown activation dtype %d", xdt);
   if (batch < 1 || batch > 8) return fail(LB_ERR_SHAPE, "batch must be in [1, 8] (got %d)", batch);
   if (!lb::aligned16(x) || !lb::aligned16(y)) return fail(LB_ERR_ALIGN, "x and y must be 16-byte aligned");
+  if (W->fmt == LB_FMT_TERNARY5_G128)
+    return lb::launch_gemv_t5(*W, x, xdt, batch, y, reinterpret_cast<cudaStream_t>(stream));
   return lb::launch_gemv(*W, x, xdt, batch, y, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -179,6 +200,8 @@ lb_status lb_gemv_batched(const lb_gemv_problem* problems, int count, int xdt, i
     if (s != LB_OK) return s;
     if (pb.W.fmt != problems[0].W.fmt)
       return fail(LB_ERR_UNSUPPORTED, "problem %d: every problem of one call must have the same format", i);
+    if (pb.W.fmt == LB_FMT_TERNARY5_G128)
+      return fail(LB_ERR_UNSUPPORTED, "lb_gemv_batched takes the 1-bit and 2-bit ternary formats");
     if (!pb.x || !pb.y) return fail(LB_ERR_NULL, "problem %d: x and y must be non-NULL", i);
     if (!lb::aligned16(pb.x) || !lb::aligned16(pb.y)) return fail(LB_ERR_ALIGN, "problem %d: x and y must be 16-byte aligned", i);
   }
@@ -192,6 +215,8 @@ lb_status lb_gemv_swiglu(const lb_weight* Wg, const lb_weight* Wu, const void* x
   s = check_weight(Wu);
   if (s != LB_OK) return s;
   if (Wg->fmt != Wu->fmt) return fail(LB_ERR_UNSUPPORTED, "gate and up must have the same format");
+  if (Wg->fmt == LB_FMT_TERNARY5_G128)
+    return fail(LB_ERR_UNSUPPORTED, "lb_gemv_swiglu takes the 1-bit and 2-bit ternary formats");
   if (Wg->n != Wu->n || Wg->k != Wu->k)
     return fail(LB_ERR_SHAPE, "gate (%lld x %lld) and up (%lld x %lld) must have the same shape", (long long)Wg->n,
                 (long long)Wg->k, (long long)Wu->n, (long long)Wu->k);
@@ -216,6 +241,7 @@ lb_status lb_gemm(const lb_weight* W, const void* x, int xdt, int64_t m, void* y
                   size_t workspace_bytes, lb_stream stream) {
   lb_status s = check_weight(W);
   if (s != LB_OK) return s;
+  if (W->fmt == LB_FMT_TERNARY5_G128) return fail(LB_ERR_UNSUPPORTED, "lb_gemm takes the 1-bit and 2-bit ternary formats");
   if (!x || !y) return fail(LB_ERR_NULL, "x and y must be non-NULL");
   if (!valid_dtype(xdt) || !valid_dtype(ydt)) return fail(LB_ERR_DTYPE, "unknown dtype (x %d, y %d)", xdt, ydt);
   if (m < 1 || m > kGemmMaxM) return fail(LB_ERR_SHAPE, "m must be in [1, %lld] (got %lld)", (long long)kGemmMaxM, (long long)m);
@@ -235,6 +261,8 @@ lb_status lb_gemm_noalloc(const lb_weight* W, const void* x, int xdt, int64_t m,
                           lb_stream stream) {
   lb_status s = check_weight(W);
   if (s != LB_OK) return s;
+  if (W->fmt == LB_FMT_TERNARY5_G128)
+    return fail(LB_ERR_UNSUPPORTED, "lb_gemm_noalloc takes the 1-bit and 2-bit ternary formats");
   if (!x || !y) return fail(LB_ERR_NULL, "x and y must be non-NULL");
   if (!valid_dtype(xdt) || !valid_dtype(ydt)) return fail(LB_ERR_DTYPE, "unknown dtype (x %d, y %d)", xdt, ydt);
   if (m < 1 || m > kGemmMaxM) return fail(LB_ERR_SHAPE, "m must be in [1, %lld] (got %lld)", (long long)kGemmMaxM, (long long)m);
@@ -249,6 +277,7 @@ lb_status lb_embed(const lb_weight* W, const int32_t* ids, int64_t count, void* 
                    lb_stream stream) {
   lb_status s = check_weight(W);
   if (s != LB_OK) return s;
+  if (W->fmt == LB_FMT_TERNARY5_G128) return fail(LB_ERR_UNSUPPORTED, "lb_embed takes the 1-bit and 2-bit ternary formats");
   if (count < 0 || count > INT32_MAX) return fail(LB_ERR_SHAPE, "count must be in [0, 2^31) (got %lld)", (long long)count);
   if (count * ((W->k + 1023) / 1024) > (int64_t(1) << 34) - 8)
     return fail(LB_ERR_SHAPE, "count x K too large for one launch (count %lld, k %lld)", (long long)count,

@@ -40,6 +40,9 @@ lb_status launch_pack_1bit(const float* w, int64_t n, int64_t k, uint8_t* codes,
 lb_status launch_pack_ternary(const int8_t* t, const uint16_t* s_in, int64_t n, int64_t k,
                               uint8_t* codes, uint16_t* scales, cudaStream_t st, uint32_t* flags_out);
 lb_status launch_gemv(const lb_weight& W, const void* x, int xdt, int batch, void* y, cudaStream_t st);
+lb_status launch_pack_ternary5(const int8_t* t, const uint16_t* s_in, int64_t n, int64_t k, uint8_t* codes,
+                               uint16_t* scales, cudaStream_t st, uint32_t* flags_out);
+lb_status launch_gemv_t5(const lb_weight& W, const void* x, int xdt, int batch, void* y, cudaStream_t st);
 lb_status launch_gemv_swiglu(const lb_weight& Wg, const lb_weight& Wu, const void* x, int xdt, int batch, void* h,
                              cudaStream_t st);
 lb_status launch_gemv_batched(const lb_gemv_problem* probs, int count, int xdt, int batch, cudaStream_t st);

@@ -18,9 +18,10 @@ LIB_PATH = os.path.join(HERE, "liblb.so")
 LB_OK = 0
 LB_FMT_1BIT_G128 = 1
 LB_FMT_TERNARY_G128 = 2
+LB_FMT_TERNARY5_G128 = 3
 LB_F16 = 1
 LB_BF16 = 2
-FORMATS = {"1bit": LB_FMT_1BIT_G128, "ternary": LB_FMT_TERNARY_G128}
+FORMATS = {"1bit": LB_FMT_1BIT_G128, "ternary": LB_FMT_TERNARY_G128, "ternary5": LB_FMT_TERNARY5_G128}
 DTYPES = {"f16": LB_F16, "bf16": LB_BF16}
 
 STATUS_NAMES = {0: "LB_OK", 1: "LB_ERR_NULL", 2: "LB_ERR_SHAPE", 3: "LB_ERR_ALIGN", 4: "LB_ERR_DTYPE",
@@ -30,7 +31,7 @@ STATUS_NAMES = {0: "LB_OK", 1: "LB_ERR_NULL", 2: "LB_ERR_SHAPE", 3: "LB_ERR_ALIG
 # Symbols declared in include/lb.h (checked by the tests against the header and the library).
 EXPORTED = ("lb_status_string", "lb_last_error", "lb_version", "lb_packed_bytes", "lb_pack_1bit",
             "lb_pack_ternary", "lb_gemv", "lb_gemm_workspace_bytes", "lb_gemm", "lb_device_error",
-            "lb_gemm_noalloc", "lb_gemv_batched", "lb_embed", "lb_gemv_swiglu")
+            "lb_gemm_noalloc", "lb_gemv_batched", "lb_embed", "lb_gemv_swiglu", "lb_pack_ternary5")
 LB_GEMM_NOALLOC_SCRATCH_BYTES = 8 << 20
 LB_GEMV_BATCH_MAX = 8
 
@@ -65,6 +66,7 @@ def _load():
         "lb_packed_bytes": ([i32, i64, i64, sz_p, sz_p], i32),
         "lb_pack_1bit": ([vp, i64, i64, vp, vp, vp], i32),
         "lb_pack_ternary": ([vp, vp, i64, i64, vp, vp, vp], i32),
+        "lb_pack_ternary5": ([vp, vp, i64, i64, vp, vp, vp], i32),
         "lb_gemv": ([ctypes.POINTER(lb_weight), vp, i32, i32, vp, vp], i32),
         "lb_gemm_workspace_bytes": ([i64, i64, i64, i32, sz_p], i32),
         "lb_gemm": ([ctypes.POINTER(lb_weight), vp, i32, i64, vp, i32, vp, ctypes.c_size_t, vp], i32),
@@ -149,6 +151,11 @@ def lb_pack_1bit(w, n: int, k: int, codes, scales, stream=None) -> None:
 def lb_pack_ternary(t, s_in, n: int, k: int, codes, scales, stream=None) -> None:
     _check(_lib.lb_pack_ternary(_ptr(t), _ptr(s_in), n, k, _ptr(codes), _ptr(scales), _stream(stream)),
            "lb_pack_ternary")
+
+
+def lb_pack_ternary5(t, s_in, n: int, k: int, codes, scales, stream=None) -> None:
+    _check(_lib.lb_pack_ternary5(_ptr(t), _ptr(s_in), n, k, _ptr(codes), _ptr(scales), _stream(stream)),
+           "lb_pack_ternary5")
 
 
 def make_weight(fmt: int, n: int, k: int, codes, scales) -> lb_weight:

@@ -65,6 +65,15 @@ def pack_ternary(t: torch.Tensor, s: torch.Tensor, stream=None) -> PackedWeight:
     return pw
 
 
+def pack_ternary5(t: torch.Tensor, s: torch.Tensor, stream=None) -> PackedWeight:
+    """int8 codes [n][k] + binary16 scales [n][k/128] -> PackedWeight, five codes per byte."""
+    assert t.is_cuda and t.dtype == torch.int8 and t.is_contiguous() and t.dim() == 2
+    n, k = t.shape
+    pw = PackedWeight.empty(lb.LB_FMT_TERNARY5_G128, n, k, device=t.device)
+    lb.lb_pack_ternary5(t, s.contiguous(), n, k, pw.codes, pw.scales, stream)
+    return pw
+
+
 def gemv(W: PackedWeight, x: torch.Tensor, y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """y[b][n] = W x[b] for x [batch][k] (batch 1..8), output in the dtype of x."""
     assert x.is_cuda and x.is_contiguous() and x.dim() == 2 and x.shape[1] == W.k

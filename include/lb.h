@@ -10,11 +10,19 @@
  *     Bonsai 27B: compilaciones ternarias y de 1 bit", section "Cómo funciona la compresión"),
  *     stored as 2-bit fields f = t + 1 (0 -> -1, 1 -> 0, 2 -> +1; 3 is invalid): 32 B of codes
  *     + 2 B of scale per 128 weights = 2.125 bits per weight.
+ *   - ternary, five per byte (LB_FMT_TERNARY5_G128; es.news.hada.io topic 31450, comments: five
+ *     three-state values fit one byte; kerneldigest.dev, "Bonsai 2 27B", section "Arquitectura
+ *     del Sistema": 1.76 effective bits per weight): the same codes as base-3 digits f = t + 1,
+ *     26 B of codes + 2 B of scale per 128 weights = 1.75 bits per weight.  Taken by
+ *     lb_pack_ternary5 and lb_gemv; the other products return LB_ERR_UNSUPPORTED for it.
  *
  * Packed layout of an N x K matrix (rows n = output features, K = reduction, K % 128 == 0),
  * two planes, both row-major and contiguous:
  *   codes : 1-bit   uint8 [N][K/8],  weight k of row n = bit (k % 8) of byte k/8 (LSB first)
  *           ternary uint8 [N][K/4],  weight k of row n = bits 2(k%4)..2(k%4)+1 of byte k/4
+ *           ternary five per byte: uint8 [N][26 K/128]; group g of row n is bytes 26g .. 26g+25,
+ *           byte j of a group holds its weights 5j .. 5j+4 as sum_i (t + 1) 3^i (first weight in
+ *           the lowest digit); byte 25 holds weights 125..127
  *   scales: uint16  [N][K/128], the binary16 bit pattern of the scale of group k/128 of row n
  *
  * Activations and outputs are row-major [rows][K] / [rows][N] arrays of binary16 (LB_F16) or
@@ -59,7 +67,7 @@ typedef enum lb_status {
   LB_ERR_WORKSPACE = 10   /* workspace pointer/size smaller than lb_gemm_workspace_bytes()    */
 } lb_status;
 
-typedef enum lb_format { LB_FMT_1BIT_G128 = 1, LB_FMT_TERNARY_G128 = 2 } lb_format;
+typedef enum lb_format { LB_FMT_1BIT_G128 = 1, LB_FMT_TERNARY_G128 = 2, LB_FMT_TERNARY5_G128 = 3 } lb_format;
 
 typedef enum lb_dtype { LB_F16 = 1, LB_BF16 = 2 } lb_dtype;
 
@@ -86,6 +94,7 @@ int lb_version(void);
  * Byte sizes of the two planes of an n x k matrix in format `fmt` (pure host arithmetic):
  *   1-bit:   codes = n*k/8, scales = n*(k/128)*2   (18 bytes per group, 7minutos.es tutorial, §7 demo)
  *   ternary: codes = n*k/4, scales = n*(k/128)*2   (34 bytes per group)
+ *   ternary five per byte: codes = n*(k/128)*26, scales = n*(k/128)*2   (28 bytes per group)
  * Errors: LB_ERR_NULL (an output pointer is NULL), LB_ERR_SHAPE, LB_ERR_DTYPE (unknown fmt).
  */
 lb_status lb_packed_bytes(int fmt, int64_t n, int64_t k, size_t* codes_bytes, size_t* scales_bytes);
@@ -120,13 +129,23 @@ lb_status lb_pack_ternary(const int8_t* t, const uint16_t* s_in, int64_t n, int6
                           uint8_t* codes, uint16_t* scales, lb_stream stream);
 
 /*
+ * The same ternary packing, five codes per byte (LB_FMT_TERNARY5_G128 layout above): byte j of a
+ * group is sum_i (t[5j+i] + 1) 3^i.  Arguments as lb_pack_ternary, with codes a device uint8
+ * [n][26 k/128] output (16-byte aligned base).  Synchronous; LB_ERR_CODE if any t is outside
+ * {-1, 0, +1}.
+ */
+lb_status lb_pack_ternary5(const int8_t* t, const uint16_t* s_in, int64_t n, int64_t k,
+                           uint8_t* codes, uint16_t* scales, lb_stream stream);
+
+/*
  * Decode GEMV and small-batch GEMV (7minutos.es, "PrismML lanza Bonsai 27B", section
  * "Rendimiento y decodificación especulativa DSpark": generation is memory-bandwidth bound;
  * speculative verification of k = 4 drafted tokens runs the target at width k + 1):
  *     y[b][n] = sum_g s[n][g] * sum_{i<128} t[n][128g+i] * x[b][128g+i],   0 <= b < batch,
  * with FP32 accumulation, rounded once to the dtype of x (round to nearest even).
  *
- * W     : packed matrix (n x k).
+ * W     : packed matrix (n x k), any format; the five-per-byte ternary format runs a CUDA-core
+ *         kernel that decodes a code byte through a 243-entry table (no K limit).
  * x     : device [batch][k] of `xdt`, 16-byte aligned.     y : device [batch][n] of `xdt`.
  * batch : 1 .. 8.
  * Asynchronous on `stream`.  Errors (no launch): LB_ERR_NULL, LB_ERR_SHAPE, LB_ERR_ALIGN,

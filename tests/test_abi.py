@@ -76,7 +76,7 @@ def test_gemv_validation():
     assert _status(lb.lb_gemv, W, A16, lb.LB_F16, 0, A16, 0) == "LB_ERR_SHAPE"
     assert _status(lb.lb_gemv, W, A16, lb.LB_F16, 9, A16, 0) == "LB_ERR_SHAPE"
     assert _status(lb.lb_gemv, W, MIS, lb.LB_F16, 1, A16, 0) == "LB_ERR_ALIGN"
-    assert _status(lb.lb_gemv, lb.make_weight(3, 16, 128, A16, A16), A16, lb.LB_F16, 1, A16, 0) == "LB_ERR_DTYPE"
+    assert _status(lb.lb_gemv, lb.make_weight(4, 16, 128, A16, A16), A16, lb.LB_F16, 1, A16, 0) == "LB_ERR_DTYPE"
     assert _status(lb.lb_gemv, lb.make_weight(1, 16, 130, A16, A16), A16, lb.LB_F16, 1, A16, 0) == "LB_ERR_SHAPE"
     assert _status(lb.lb_gemv, lb.make_weight(1, 16, 128, MIS, A16), A16, lb.LB_F16, 1, A16, 0) == "LB_ERR_ALIGN"
     assert _status(lb.lb_gemv, lb.make_weight(1, 16, 128, None, A16), A16, lb.LB_F16, 1, A16, 0) == "LB_ERR_NULL"
@@ -103,6 +103,22 @@ def test_gemm_validation():
     assert _status(lb.lb_gemm, Wk, A16, lb.LB_BF16, 1 << 20, A16, lb.LB_BF16, A16, need, 0) == "LB_ERR_SHAPE"
 
 
+def test_ternary5_entry_points():
+    """The five-per-byte format: sizes, packer validation, and the products that do not take it."""
+    assert lb.lb_packed_bytes(lb.LB_FMT_TERNARY5_G128, 3, 1024) == (3 * 8 * 26, 3 * 8 * 2)
+    assert _status(lb.lb_pack_ternary5, A16, A16, 4, 100, A16, A16) == "LB_ERR_SHAPE"
+    assert _status(lb.lb_pack_ternary5, None, A16, 4, 128, A16, A16) == "LB_ERR_NULL"
+    assert _status(lb.lb_pack_ternary5, A16, A16, 4, 128, MIS, A16) == "LB_ERR_ALIGN"
+    W5 = lb.make_weight(lb.LB_FMT_TERNARY5_G128, 256, 256, A16, A16)
+    need = lb.lb_gemm_workspace_bytes(5, 256, 256, lb.LB_BF16)
+    assert _status(lb.lb_gemm, W5, A16, lb.LB_BF16, 5, A16, lb.LB_BF16, A16, need, 0) == "LB_ERR_UNSUPPORTED"
+    assert _status(lb.lb_gemm_noalloc, W5, A16, lb.LB_BF16, 5, A16, lb.LB_BF16) == "LB_ERR_UNSUPPORTED"
+    assert _status(lb.lb_embed, W5, A16, 3, A16, lb.LB_BF16, 0) == "LB_ERR_UNSUPPORTED"
+    assert _status(lb.lb_gemv_batched, [(W5, A16, A16)], lb.LB_F16, 1) == "LB_ERR_UNSUPPORTED"
+    assert _status(lb.lb_gemv_swiglu, W5, W5, A16, lb.LB_F16, 1, A16, 0) == "LB_ERR_UNSUPPORTED"
+    assert _status(lb.lb_gemv, W5, A16, lb.LB_F16, 9, A16, 0) == "LB_ERR_SHAPE"
+
+
 def test_embed_validation():
     W = lb.make_weight(lb.LB_FMT_1BIT_G128, 64, 256, A16, A16)
     assert _status(lb.lb_embed, W, A16, 0, None, lb.LB_BF16, 0) == "LB_OK"            # nothing to do
@@ -115,7 +131,7 @@ def test_embed_validation():
     assert _status(lb.lb_embed, W, A16, 3, A16, 7, 0) == "LB_ERR_DTYPE"
     assert _status(lb.lb_embed, W, A16 + 2, 3, A16, lb.LB_F16, 0) == "LB_ERR_ALIGN"     # ids: 4-byte
     assert _status(lb.lb_embed, W, A16, 3, A16 + 8, lb.LB_F16, 0) == "LB_ERR_ALIGN"     # out: 16-byte
-    assert _status(lb.lb_embed, lb.make_weight(3, 64, 256, A16, A16), A16, 3, A16, lb.LB_F16, 0) == "LB_ERR_DTYPE"
+    assert _status(lb.lb_embed, lb.make_weight(4, 64, 256, A16, A16), A16, 3, A16, lb.LB_F16, 0) == "LB_ERR_DTYPE"
     assert _status(lb.lb_embed, lb.make_weight(2, 64, 200, A16, A16), A16, 3, A16, lb.LB_F16, 0) == "LB_ERR_SHAPE"
 
 
