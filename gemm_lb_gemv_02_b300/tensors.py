@@ -6,6 +6,7 @@ method happens here.
 
 from __future__ import annotations
 
+import contextlib
 from dataclasses import dataclass, field
 
 import torch
@@ -13,6 +14,14 @@ import torch
 from . import lb
 
 _TORCH = {lb.LB_F16: torch.float16, lb.LB_BF16: torch.bfloat16}
+
+
+def _alloc_on(stream):
+    """Context for allocating a call's outputs and workspace: a torch stream owns what is allocated
+    under it, so torch's caching allocator does not hand the memory to another stream while the
+    call's kernels may still use it.  A raw stream handle (or None) allocates on the current
+    stream, and keeping those buffers alive is then the caller's job."""
+    return torch.cuda.stream(stream) if isinstance(stream, torch.cuda.Stream) else contextlib.nullcontext()
 
 
 def dtype_code(t: torch.dtype) -> int:
@@ -78,7 +87,8 @@ def gemv(W: PackedWeight, x: torch.Tensor, y: torch.Tensor | None = None, stream
     """y[b][n] = W x[b] for x [batch][k] (batch 1..8), output in the dtype of x."""
     assert x.is_cuda and x.is_contiguous() and x.dim() == 2 and x.shape[1] == W.k
     if y is None:
-        y = torch.empty(x.shape[0], W.n, dtype=x.dtype, device=x.device)
+        with _alloc_on(stream):
+            y = torch.empty(x.shape[0], W.n, dtype=x.dtype, device=x.device)
     lb.lb_gemv(W.struct(), x, dtype_code(x.dtype), x.shape[0], y, stream)
     return y
 
@@ -90,7 +100,8 @@ def gemv_batched(problems, ys=None, stream=None) -> list:
     x0 = problems[0][1]
     batch, dt = x0.shape[0], x0.dtype
     if ys is None:
-        ys = [torch.empty(batch, W.n, dtype=dt, device=x.device) for W, x in problems]
+        with _alloc_on(stream):
+            ys = [torch.empty(batch, W.n, dtype=dt, device=x.device) for W, x in problems]
     for W, x in problems:
         assert x.is_cuda and x.is_contiguous() and x.dim() == 2 and x.shape == (batch, W.k) and x.dtype == dt
     lb.lb_gemv_batched([(W.struct(), x, y) for (W, x), y in zip(problems, ys)], dtype_code(dt), batch, stream)
@@ -102,7 +113,8 @@ def gemv_swiglu(Wg: PackedWeight, Wu: PackedWeight, x: torch.Tensor, h: torch.Te
     """h[b] = silu(Wg x[b]) * (Wu x[b]) for x [batch][k] (batch 1..8), output in the dtype of x."""
     assert x.is_cuda and x.is_contiguous() and x.dim() == 2 and x.shape[1] == Wg.k
     if h is None:
-        h = torch.empty(x.shape[0], Wg.n, dtype=x.dtype, device=x.device)
+        with _alloc_on(stream):
+            h = torch.empty(x.shape[0], Wg.n, dtype=x.dtype, device=x.device)
     lb.lb_gemv_swiglu(Wg.struct(), Wu.struct(), x, dtype_code(x.dtype), x.shape[0], h, stream)
     return h
 
@@ -113,11 +125,12 @@ def gemm(W: PackedWeight, x: torch.Tensor, out_dtype: torch.dtype = torch.bfloat
     assert x.is_cuda and x.is_contiguous() and x.dim() == 2 and x.shape[1] == W.k
     m = x.shape[0]
     xdt = dtype_code(x.dtype)
-    if y is None:
-        y = torch.empty(m, W.n, dtype=out_dtype, device=x.device)
     need = lb.lb_gemm_workspace_bytes(m, W.n, W.k, xdt)
-    if workspace is None or workspace.numel() < need:
-        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    with _alloc_on(stream):
+        if y is None:
+            y = torch.empty(m, W.n, dtype=out_dtype, device=x.device)
+        if workspace is None or workspace.numel() < need:
+            workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
     lb.lb_gemm(W.struct(), x, xdt, m, y, dtype_code(y.dtype), workspace, workspace.numel(), stream)
     return y
 
@@ -128,7 +141,8 @@ def embed(W: PackedWeight, ids: torch.Tensor, out_dtype: torch.dtype = torch.bfl
     assert ids.is_cuda and ids.dtype == torch.int32 and ids.is_contiguous() and ids.dim() == 1
     count = ids.shape[0]
     if out is None:
-        out = torch.empty(count, W.k, dtype=out_dtype, device=ids.device)
+        with _alloc_on(stream):
+            out = torch.empty(count, W.k, dtype=out_dtype, device=ids.device)
     assert out.is_cuda and out.is_contiguous() and out.shape == (count, W.k)
     lb.lb_embed(W.struct(), ids, count, out, dtype_code(out.dtype), stream)
     return out
