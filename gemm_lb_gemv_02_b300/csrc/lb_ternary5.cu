@@ -85,6 +85,15 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_t5_kernel(const uint8_t* __r
   }
   // lane l: byte l of each group; its digits i < nd are weights 5l + i
   const int nd = lane < 25 ? 5 : (lane == 25 ? 3 : 0);
+  // this warp's rows (rows past n read row n - 1 and are not stored): code and scale row starts
+  const uint8_t* crow[kRowsPerWarp];
+  const uint16_t* srow[kRowsPerWarp];
+#pragma unroll
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+    const int64_t row = min(row0 + r, n - 1);
+    crow[r] = codes + row * G * kT5Bytes + lane;
+    srow[r] = scales + row * G;
+  }
   float acc[kRowsPerWarp][BP];
 #pragma unroll
   for (int r = 0; r < kRowsPerWarp; ++r)
@@ -117,9 +126,8 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_t5_kernel(const uint8_t* __r
       if (gl >= ng) return;
 #pragma unroll
       for (int r = 0; r < kRowsPerWarp; ++r) {
-        const int64_t row = min(row0 + r, n - 1);
-        c[r] = __ldg(codes + row * G * kT5Bytes + (g0 + gl) * kT5Bytes + lane);
-        sv[r] = __ldg(scales + row * G + g0 + gl);
+        c[r] = __ldg(crow[r] + (g0 + gl) * kT5Bytes);
+        sv[r] = __ldg(srow[r] + g0 + gl);
       }
     };
     auto group = [&](int gl, const uint32_t (&c)[kRowsPerWarp], const uint32_t (&sv)[kRowsPerWarp]) {
