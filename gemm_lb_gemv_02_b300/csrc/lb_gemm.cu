@@ -18,23 +18,26 @@
 //     match the decoder's register order, written as ready-made 128-byte-swizzled shared-memory
 //     images of 128-token x 64 tiles (one 16 KB contiguous block per tile), so that one bulk copy
 //     moves a tile;
-//   * warp 8 (one lane): after griddepcontrol.wait, bulk-copies the token rows of one or two such
-//     tiles per stage into a ring 10 (one tile) or 5 (two tiles) stages deep (mbarrier complete_tx);
-//   * warp 10 (one lane): TMA-loads the CTA's packed codes, 128 rows x 128 bytes per chunk (512 K of
+//   * warp 16 (one lane): after griddepcontrol.wait, bulk-copies the token rows of one or two such
+//     tiles per stage into the stage ring (mbarrier complete_tx);
+//   * warp 18 (one lane): TMA-loads the CTA's packed codes, 128 rows x 128 bytes per chunk (512 K of
 //     ternary, 1024 K of 1-bit), into a CR-deep ring, so the decoders read their codes from shared
 //     memory long after the HBM latency was paid;
-//   * warp 11: the group scales, 128 rows x 8 groups per chunk, into an SR-deep ring: one TMA per
+//   * warp 19: the group scales, 128 rows x 8 groups per chunk, into an SR-deep ring: one TMA per
 //     chunk when a scale row is a multiple of 16 bytes, otherwise 32 lanes load and store them;
-//   * warps 0-7: warp w owns TMEM lanes 32(w % 4) .. +31 (weight rows n0 + lane) and half of each
-//     stage's K; it decodes its codes with the group scale (a LOP3 and two half2 operations per two
-//     ternary weights, one LOP3 per two 1-bit weights) and stores the stage's A columns with
-//     tcgen05.st;
-//   * warp 9: allocates TMEM (an 8-stage ring of 32 A columns + a 256-column FP32 accumulator), one
+//   * warps 0-15: two groups of 8 take alternate stages; in a group, warp w owns TMEM lanes
+//     32(w % 4) .. +31 (weight rows n0 + lane) and half of the stage's K; it decodes its codes with
+//     the group scale (a LOP3 and two half2 operations per two ternary weights, one LOP3 per two
+//     1-bit weights), stores the stage's A columns with tcgen05.st and publishes the store after it
+//     has decoded its next stage;
+//   * warp 17: allocates TMEM (an 8-stage ring of 32 A columns + a 256-column FP32 accumulator); one
 //     lane issues tcgen05.mma kind::f16 (M128, N = the tile's tokens rounded up to 16, K16, A from
-//     TMEM) and commits each stage's activation slot and A slot back separately, so neither ring
-//     waits on the other's latency;
-//   * epilogue: warps 0-7 read the accumulator with tcgen05.ld (lane = weight row, column =
-//     token) and store BF16/FP16 Y[token][row].
+//     TMEM): one wait and four MMAs per stage;
+//   * one stage ring (8 stages with one activation tile, 5 with two) carries both operands: its full
+//     barrier counts the 8 decoder warps of the stage plus the activation bytes, and one commit
+//     per stage frees the TMEM columns and the activation slot together;
+//   * epilogue: warps 0-15 read the accumulator with tcgen05.ld (lane = weight row, 64 tokens per
+//     warp) and store BF16/FP16 Y[token][row].
 // The GEMM is launched with programmatic dependent launch, so the weight decode of the first
 // stages overlaps the activation prologue.  Every mbarrier wait is bounded; a timeout sets a bit in
 // the device error word and the CTA finishes (TMEM is always released).

@@ -34,6 +34,11 @@
 // partial sums meet in distributed shared memory.  The kernel is launched with programmatic
 // dependent launch: weight loads start before griddepcontrol.wait, which guards every read of x
 // and write of y.
+//
+// Launch modes (the problem table in the kernel's arguments): one GEMV with persistent CTAs; up to
+// 8 GEMVs in one launch with one CTA (or cluster) per (problem, row block); and the SiLU-gated
+// pair, in which one CTA (or cluster) runs a row block of the gate matrix and then the same row
+// block of the up matrix on one x prologue and writes h = silu(g) * u (g and u stay in FP32).
 #include <cuda.h>
 
 #include <cstring>

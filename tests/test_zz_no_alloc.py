@@ -3,8 +3,8 @@
 Plug-in style hosts that hand a kernel only its input and output buffers, and serving loops that
 must not call cudaMalloc (it can synchronise the device), cannot give lb_gemm a workspace; this
 entry point stages activations in a scratch array owned by the library instead.  The test calls it
-through the C ABI twice in a row, on different inputs, and checks each result against lb_gemm's
-on the same inputs within the tolerance the other tests use.  It is collected last so that a run
+through the C ABI twice in a row, on different inputs and for both formats, and checks each
+result bit for bit against lb_gemm's on the same inputs and against the oracle's bound.  It is collected last so that a run
 stopping at the first failure has already run everything else.
 """
 
@@ -35,24 +35,34 @@ def _noalloc(pw, x, out_dtype):
     return y
 
 
-def test_noalloc_matches_gemm_on_two_calls():
+@pytest.mark.parametrize("fmt", ["1bit", "ternary"])
+def test_noalloc_matches_gemm_on_two_calls(fmt):
+    """Same kernels, same staging layout: the result equals lb_gemm's bit for bit, and both are
+    within the product bound of the oracle."""
     n, k = 512, 1280
-    t = synth.ternary_codes(n, k, seed=71)
-    s = synth.ternary_scales_bits(n, k, 0.02, seed=72)
-    pw = tensors.pack_ternary(t.cuda(), s.cuda())
-    codes, scales = orc.pack_ternary(t.numpy(), s.numpy().view(np.uint16))
+    if fmt == "1bit":
+        w = synth.weights_fp32(n, k, 0.05, seed=70)
+        pw = tensors.pack_1bit(w.cuda())
+        codes, scales = orc.pack_1bit(w.numpy())
+        f = orc.FMT_1BIT
+    else:
+        t = synth.ternary_codes(n, k, seed=71)
+        s = synth.ternary_scales_bits(n, k, 0.02, seed=72)
+        pw = tensors.pack_ternary(t.cuda(), s.cuda())
+        codes, scales = orc.pack_ternary(t.numpy(), s.numpy().view(np.uint16))
+        f = orc.FMT_TERNARY
     for call, (m, xdt, out) in enumerate(((300, "bf16", torch.bfloat16), (130, "f16", torch.float16))):
         x = synth.activations(m, k, xdt, seed=73 + call).cuda()
-        y_ref = tensors.gemm(pw, x, out_dtype=out)          # the existing entry point
+        y_gemm = tensors.gemm(pw, x, out_dtype=out)          # the existing entry point
         y = _noalloc(pw, x, out)
         torch.cuda.synchronize()
         assert lb.lb_device_error(clear=True) == 0
+        assert np.array_equal(u16(y), u16(y_gemm)), f"call {call}: noalloc differs from lb_gemm"
         dt = "bf16" if out == torch.bfloat16 else "f16"
         xv = orc.decode_activation_bits(u16(x), xdt)
-        _, a = orc.gemm(orc.FMT_TERNARY, codes, scales, k, xv)
+        y_ref, a = orc.gemm(f, codes, scales, k, xv)
         yv = orc.decode_activation_bits(u16(y), dt)
-        yr = orc.decode_activation_bits(u16(y_ref), dt)
-        assert orc.within_tolerance(yv, yr, a, dt).all(), f"call {call}: noalloc differs from lb_gemm"
+        assert orc.within_tolerance(yv, y_ref, a, dt).all(), f"call {call}: outside the product bound"
 
 
 def test_noalloc_rejects_oversized_request():
