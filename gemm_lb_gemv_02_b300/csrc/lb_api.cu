@@ -1,4 +1,5 @@
 // liblb C ABI: argument validation, error reporting and dispatch to the kernel launchers.
+#include <atomic>
 #include <climits>
 #include <cstdarg>
 #include <cstdio>
@@ -17,6 +18,7 @@ __device__ uint32_t g_device_error;
 
 constexpr int kMaxDevices = 64;
 uint32_t* g_error_ptr[kMaxDevices] = {};
+unsigned long long g_error_ctx[kMaxDevices] = {};
 std::mutex g_error_ptr_mutex;
 
 }  // namespace
@@ -45,16 +47,53 @@ int sm_count() {
   return n;
 }
 
+// Unique id of the calling thread's current CUDA context (cuCtxGetId ids are never reused within a
+// process, unlike context handles), or 0 if the driver cannot report one.  A cached device address of
+// a module-scope __device__ variable is valid only for the context it was taken in: after
+// cudaDeviceReset the module is loaded again, possibly elsewhere.
+unsigned long long context_id() {
+  typedef CUresult (*GetCurrentFn)(CUcontext*);
+  typedef CUresult (*GetIdFn)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
 uint32_t* device_error_word() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  const unsigned long long ctx = context_id();
   std::lock_guard<std::mutex> lk(g_error_ptr_mutex);
-  if (!g_error_ptr[dev]) {
+  if (!g_error_ptr[dev] || ctx == 0 || ctx != g_error_ctx[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
     g_error_ptr[dev] = static_cast<uint32_t*>(p);
+    g_error_ctx[dev] = ctx;
   }
   return g_error_ptr[dev];
+}
+
+std::atomic<int> g_test_fault{0};
+
+bool take_test_fault(int kernel) {
+  int expected = kernel;
+  return g_test_fault.load(std::memory_order_relaxed) == kernel &&
+         g_test_fault.compare_exchange_strong(expected, 0);
 }
 
 }  // namespace lb
@@ -86,10 +125,8 @@ lb_status check_weight(const lb_weight* W) {
 
 bool valid_dtype(int d) { return d == LB_F16 || d == LB_BF16; }
 
-// Launch-shape limits of the GEMM: 65535 token tiles of 256 along grid y; the activation prologue
-// runs one thread per 16 activations, at most 2^31 - 1 blocks of 256 threads.
+// Launch-shape limit of the GEMM: 65535 token tiles of 256 along grid y.
 constexpr int64_t kGemmMaxM = int64_t(65535) * 256;
-constexpr int64_t kGemmMaxMK = (int64_t(1) << 31) * 4096 - 4096;
 
 }  // namespace
 
@@ -245,8 +282,6 @@ lb_status lb_gemm(const lb_weight* W, const void* x, int xdt, int64_t m, void* y
   if (!x || !y) return fail(LB_ERR_NULL, "x and y must be non-NULL");
   if (!valid_dtype(xdt) || !valid_dtype(ydt)) return fail(LB_ERR_DTYPE, "unknown dtype (x %d, y %d)", xdt, ydt);
   if (m < 1 || m > kGemmMaxM) return fail(LB_ERR_SHAPE, "m must be in [1, %lld] (got %lld)", (long long)kGemmMaxM, (long long)m);
-  if ((m + 127) / 128 * 128 * W->k > kGemmMaxMK)
-    return fail(LB_ERR_SHAPE, "m x k too large for one call (m %lld, k %lld)", (long long)m, (long long)W->k);
   if (W->n % 16) return fail(LB_ERR_SHAPE, "lb_gemm needs n %% 16 == 0 (got %lld)", (long long)W->n);
   if (!lb::aligned16(x) || !lb::aligned16(y)) return fail(LB_ERR_ALIGN, "x and y must be 16-byte aligned");
   const size_t need = lb::gemm_workspace_bytes(m, W->k);
@@ -266,8 +301,6 @@ lb_status lb_gemm_noalloc(const lb_weight* W, const void* x, int xdt, int64_t m,
   if (!x || !y) return fail(LB_ERR_NULL, "x and y must be non-NULL");
   if (!valid_dtype(xdt) || !valid_dtype(ydt)) return fail(LB_ERR_DTYPE, "unknown dtype (x %d, y %d)", xdt, ydt);
   if (m < 1 || m > kGemmMaxM) return fail(LB_ERR_SHAPE, "m must be in [1, %lld] (got %lld)", (long long)kGemmMaxM, (long long)m);
-  if ((m + 127) / 128 * 128 * W->k > kGemmMaxMK)
-    return fail(LB_ERR_SHAPE, "m x k too large for one call (m %lld, k %lld)", (long long)m, (long long)W->k);
   if (W->n % 16) return fail(LB_ERR_SHAPE, "lb_gemm_noalloc needs n %% 16 == 0 (got %lld)", (long long)W->n);
   if (!lb::aligned16(x) || !lb::aligned16(y)) return fail(LB_ERR_ALIGN, "x and y must be 16-byte aligned");
   return lb::launch_gemm_noalloc(*W, x, xdt, m, y, ydt, reinterpret_cast<cudaStream_t>(stream));
@@ -288,6 +321,24 @@ lb_status lb_embed(const lb_weight* W, const int32_t* ids, int64_t count, void* 
   if (!lb::aligned16(out) || (reinterpret_cast<uintptr_t>(ids) & 3u))
     return fail(LB_ERR_ALIGN, "out must be 16-byte aligned and ids 4-byte aligned");
   return lb::launch_embed(*W, ids, count, out, out_dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+lb_status lb_read_probe(const void* data, size_t bytes, uint32_t* sink, lb_stream stream) {
+  if (bytes == 0) return LB_OK;
+  if (!data || !sink) return fail(LB_ERR_NULL, "data and sink must be non-NULL");
+  if (!lb::aligned16(data) || (reinterpret_cast<uintptr_t>(sink) & 3u))
+    return fail(LB_ERR_ALIGN, "data must be 16-byte and sink 4-byte aligned");
+  if (bytes % 16) return fail(LB_ERR_SHAPE, "bytes must be a multiple of 16 (got %zu)", bytes);
+  return lb::launch_read_probe(data, bytes, sink, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// Test-only (not declared in lb.h): make the next GEMV (kernel 1) or GEMM (kernel 2) launch of this
+// process give up its pipeline waits after a short bound; 0 clears the setting.
+lb_status lb_testing_fault_next_launch(int kernel) {
+  if (kernel != 0 && kernel != lb::kTestFaultGemv && kernel != lb::kTestFaultGemm)
+    return fail(LB_ERR_UNSUPPORTED, "unknown kernel %d", kernel);
+  lb::g_test_fault.store(kernel);
+  return LB_OK;
 }
 
 lb_status lb_device_error(uint32_t* word, int clear) {

@@ -30,9 +30,24 @@ EncodeTiledFn tensor_map_encoder();
 
 // Device word with sticky error bits (see lb_device_error); one per device, owned by lb_api.cu.
 uint32_t* device_error_word();
+// Unique id of the current CUDA context (0 if unknown); device addresses of module-scope variables
+// are cached per context id.
+unsigned long long context_id();
 constexpr uint32_t kErrGemmTimeout = 1u;        // a GEMM pipeline wait gave up
-constexpr uint32_t kErrGemmInputRange = 2u;     // a GEMM activation did not fit binary16
 constexpr uint32_t kErrEmbedId = 4u;            // an embedding row id outside [0, n)
+
+// Bound of every mbarrier wait in a kernel, and the short bound of a launch that tests the give-up
+// path (see take_test_fault).
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint64_t kTestWaitNs = 1000000ull;
+// Test-only switch, off unless a test sets it through lb_testing_fault_next_launch (exported for the
+// test suite, not declared in lb.h): the next launch of the named kernel issues none of its
+// asynchronous copies and waits with the short bound, so that every pipeline wait runs out and the
+// kernel's give-up path (error bit, no compute, cluster barriers joined, TMEM released) executes.
+// take_test_fault returns true once per setting.
+constexpr int kTestFaultGemv = 1;
+constexpr int kTestFaultGemm = 2;
+bool take_test_fault(int kernel);
 
 // Launchers implemented by the kernel translation units.  They assume validated arguments.
 lb_status launch_pack_1bit(const float* w, int64_t n, int64_t k, uint8_t* codes, uint16_t* scales,
@@ -53,6 +68,7 @@ lb_status launch_embed(const lb_weight& W, const int32_t* ids, int64_t count, vo
                        cudaStream_t st);
 lb_status launch_gemm_noalloc(const lb_weight& W, const void* x, int xdt, int64_t m, void* y, int ydt,
                               cudaStream_t st);
+lb_status launch_read_probe(const void* data, size_t bytes, uint32_t* sink, cudaStream_t st);
 
 // Pack validation bits reported by the pack kernels.
 constexpr uint32_t kPackNonFinite = 1u;

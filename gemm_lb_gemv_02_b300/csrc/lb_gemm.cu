@@ -62,64 +62,107 @@ constexpr uint32_t kAcc = 256;                    // first accumulator column
 constexpr int CR = 3, C_BYTES = WM * 128;         // code ring: chunks of 128 rows x 128 bytes
 constexpr int SR = 4, S_BYTES = WM * 16;          // scale ring: chunks of 128 rows x 8 groups
 constexpr int kBars = 2 * DMAX + 1 + 2 * CR + 2 * SR;
-constexpr size_t kSmemBytes = 1024 + XR_BYTES + CR * C_BYTES + SR * S_BYTES + kBars * 8 + 16;
+constexpr size_t kSmemBytes = 1024 + XR_BYTES + CR * C_BYTES + SR * S_BYTES + kBars * 8 + 16 + TN * 4;
 static_assert(kSmemBytes <= 232448, "shared memory per block");
 static_assert(DMAX * 32 <= 256, "A ring and accumulator share 512 TMEM columns");
 
 // ------------------------------------------------------------------------------- prologue
-// One thread per (row, SPAN-wide K block) of activations -> binary16.  The pair order matches the
-// decoder's registers: ternary (SPAN 16) puts elements p / p + 8 at positions 2p / 2p + 1; 1-bit
-// (SPAN 32) puts elements r / r + 16 at positions 2r / 2r + 1.  The 16-byte chunks go to their
-// 128-byte-swizzled slots of the 128-token x 64 tile image.
+// One CTA per token row (rows m .. mpad - 1 are the zero padding of the last tile).  bfloat16 rows
+// are scaled by an exact power of two 2^p chosen so that the row's largest magnitude lies in
+// [2^15, 2^16) (|p| <= 126), then converted to binary16: every element within 2^32 of the row
+// maximum is then exact (a bfloat16 value has 8 significant bits, and binary16 holds 8 bits down
+// to 2^-17), smaller ones round to the binary16 subnormal grid (an error of at most 2^-25 in the
+// scaled units), and nothing overflows.  The row's factor 2^-p goes to fac[row] for the epilogue;
+// binary16 rows are copied unchanged (factor 1).  The K order inside each 16- (ternary) or 32-block
+// (1-bit) matches the decoder's registers: ternary (SPAN 16) puts elements p / p + 8 at positions
+// 2p / 2p + 1; 1-bit (SPAN 32) puts elements r / r + 16 at positions 2r / 2r + 1.  The 16-byte
+// chunks go to their 128-byte-swizzled slots of the 128-token x 64 tile image.
 template <bool BF, int FMT>
 __global__ void __launch_bounds__(256) xprep_kernel(const uint16_t* __restrict__ x, int64_t m, int k,
-                                                    int64_t total, uint8_t* __restrict__ ws,
-                                                    uint32_t* __restrict__ err) {
+                                                    uint8_t* __restrict__ ws, float* __restrict__ fac) {
   constexpr int SPAN = FMT == 1 ? 32 : 16;
   constexpr int NW = SPAN / 2;                                   // 32-bit words per block
+  constexpr int CACHE = FMT == 1 ? 1 : 2;                        // blocks a thread keeps in registers
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // the GEMM may start decoding weights
-  const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (gid >= total) return;
+  __shared__ uint32_t warp_max[8];
+  const int64_t row = blockIdx.x;
+  const bool live = row < m;
   const int kb = k / SPAN;
-  const int64_t row = gid / kb;
-  const int blk = static_cast<int>(gid - row * kb);
   const int64_t mt = row / BM;
   const int r = static_cast<int>(row - mt * BM);
-  const int kt = blk / (BK / SPAN), b = blk % (BK / SPAN);
   const int KT = k / BK;
-  uint32_t X[NW];
-  if (row < m) {
-    const uint4* src = reinterpret_cast<const uint4*>(x + row * k + SPAN * blk);
+  const uint4* src_row = reinterpret_cast<const uint4*>(x + row * k);
+  auto load = [&](int blk, uint32_t (&X)[NW]) {
+    if (live && blk < kb) {
 #pragma unroll
-    for (int i = 0; i < NW / 4; ++i) {
-      const uint4 v = __ldg(src + i);
-      X[4 * i] = v.x; X[4 * i + 1] = v.y; X[4 * i + 2] = v.z; X[4 * i + 3] = v.w;
+      for (int i = 0; i < NW / 4; ++i) {
+        const uint4 v = __ldg(src_row + (SPAN / 8) * blk + i);
+        X[4 * i] = v.x; X[4 * i + 1] = v.y; X[4 * i + 2] = v.z; X[4 * i + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < NW; ++i) X[i] = 0u;
     }
-    if (BF) {
-      bool inf = false;
+  };
+  uint32_t C[CACHE][NW];                                         // blocks threadIdx.x + 256 c
+#pragma unroll
+  for (int c = 0; c < CACHE; ++c) load(threadIdx.x + 256 * c, C[c]);
+  float sc = 1.f;
+  if (BF && live) {
+    uint32_t mx = 0;
+    auto fold = [&](const uint32_t (&X)[NW]) {
+#pragma unroll
+      for (int i = 0; i < NW; ++i) mx = max(mx, max((X[i] << 16) & 0x7f800000u, X[i] & 0x7f800000u));
+    };
+#pragma unroll
+    for (int c = 0; c < CACHE; ++c) fold(C[c]);
+    for (int blk = threadIdx.x + 256 * CACHE; blk < kb; blk += 256) {   // rows longer than the cache
+      uint32_t X[NW];
+      load(blk, X);
+      fold(X);
+    }
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    mx = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) mx = max(mx, warp_max[w]);      // exponent fields order like magnitudes
+    const int e = static_cast<int>(mx >> 23) - 127;              // -127: zero or subnormal maximum
+    const int p = min(126, max(-126, 15 - e));
+    sc = __uint_as_float(static_cast<uint32_t>(127 + p) << 23);
+    if (threadIdx.x == 0) fac[row] = __uint_as_float(static_cast<uint32_t>(127 - p) << 23);
+  } else if (threadIdx.x == 0) {
+    fac[row] = 1.f;
+  }
+  auto emit = [&](int blk, uint32_t (&X)[NW]) {
+    if (blk >= kb) return;
+    const int kt = blk / (BK / SPAN), b = blk % (BK / SPAN);
+    if (BF && live) {
 #pragma unroll
       for (int i = 0; i < NW; ++i) {
-        const float lo = __uint_as_float(X[i] << 16), hi = __uint_as_float(X[i] & 0xffff0000u);
+        const float lo = __uint_as_float(X[i] << 16) * sc, hi = __uint_as_float(X[i] & 0xffff0000u) * sc;
         const __half2 h = __floats2half2_rn(lo, hi);
-        inf |= __hisinf(__low2half(h)) || __hisinf(__high2half(h));
         X[i] = *reinterpret_cast<const uint32_t*>(&h);
       }
-      if (inf) atomicOr(err, lb::kErrGemmInputRange);
     }
-  } else {
+    // output word j = (element j, element j + SPAN/2)
+    uint32_t P[NW];
 #pragma unroll
-    for (int i = 0; i < NW; ++i) X[i] = 0u;
+    for (int j = 0; j < NW; ++j) P[j] = __byte_perm(X[j >> 1], X[(j >> 1) + NW / 2], (j & 1) ? 0x7632 : 0x5410);
+    uint8_t* tile = ws + (static_cast<size_t>(mt) * KT + kt) * A_BYTES + r * 128;
+    const int sw = r & 7;
+#pragma unroll
+    for (int c = 0; c < NW / 4; ++c)
+      *reinterpret_cast<uint4*>(tile + ((((NW / 4) * b + c) ^ sw) << 4)) =
+          make_uint4(P[4 * c], P[4 * c + 1], P[4 * c + 2], P[4 * c + 3]);
+  };
+#pragma unroll
+  for (int c = 0; c < CACHE; ++c) emit(threadIdx.x + 256 * c, C[c]);
+  for (int blk = threadIdx.x + 256 * CACHE; blk < kb; blk += 256) {
+    uint32_t X[NW];
+    load(blk, X);
+    emit(blk, X);
   }
-  // output word j = (element j, element j + SPAN/2)
-  uint32_t P[NW];
-#pragma unroll
-  for (int j = 0; j < NW; ++j) P[j] = __byte_perm(X[j >> 1], X[(j >> 1) + NW / 2], (j & 1) ? 0x7632 : 0x5410);
-  uint8_t* tile = ws + (static_cast<size_t>(mt) * KT + kt) * A_BYTES + r * 128;
-  const int sw = r & 7;
-#pragma unroll
-  for (int c = 0; c < NW / 4; ++c)
-    *reinterpret_cast<uint4*>(tile + ((((NW / 4) * b + c) ^ sw) << 4)) =
-        make_uint4(P[4 * c], P[4 * c + 1], P[4 * c + 2], P[4 * c + 3]);
 }
 
 // ------------------------------------------------------------------------------- B decode
@@ -189,9 +232,9 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 template <int FMT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_lowbit_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_scales,
-                       const uint8_t* __restrict__ ws_x, const uint16_t* __restrict__ scales,
-                       uint16_t* __restrict__ y, int m, int mpad, int n, int k, int scales_tma, int y_bf16,
-                       uint32_t* __restrict__ err) {
+                       const uint8_t* __restrict__ ws_x, const float* __restrict__ fac,
+                       const uint16_t* __restrict__ scales, uint16_t* __restrict__ y, int m, int mpad, int n, int k,
+                       int scales_tma, int y_bf16, uint32_t* __restrict__ err, uint64_t wait_ns, int test_fault) {
   constexpr int RB = FMT == 1 ? 8 : 16;                            // code bytes per row per 64-K stage
   constexpr int SPC = 128 / RB;                                    // stages per code chunk (even)
   extern __shared__ uint8_t smem_raw[];
@@ -208,6 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_full = c_empty + CR;
   uint64_t* s_empty = s_full + SR;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_empty + SR);
+  float* sfac = reinterpret_cast<float*>(tmem_slot + 4);        // the tile's token factors (TN)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * WM;
@@ -251,6 +295,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpX) {
     // ---------------- activation producer (the prologue kernel wrote the tiles)
     griddep_wait();
+    // the tile's per-token factors for the epilogue; the stage barriers, the last commit and the
+    // epilogue's wait order these stores before the epilogue's loads
+    for (int i = lane; i < TN; i += 32) sfac[i] = t0 + i < mpad ? fac[t0 + i] : 0.f;
+    __syncwarp();                                  // the whole warp's stores precede lane 0's arrivals
     if (lane == 0) {
       // only the token rows the MMA reads (nmma rows of 128 bytes; the second tile's rows follow
       // the first tile's 128)
@@ -260,8 +308,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const size_t mt0 = static_cast<size_t>(t0 / BM);
       int it = 0, s = 0;
       uint32_t ph = 0;
-      for (; it < KT; ++it) {
-        if (!lbdev::mbar_wait(&empty[s], ph ^ 1)) { ok = false; break; }
+      for (; it < KT && !test_fault; ++it) {          // test_fault: issue nothing, so every wait gives up
+        if (!lbdev::mbar_wait(&empty[s], ph ^ 1, wait_ns)) { ok = false; break; }
         lbdev::mbar_arrive_expect_tx(&full[s], bytes);
         for (int tt = 0; tt < ntiles; ++tt)
           lbdev::bulk_g2s(sX + s * x_slot + tt * A_BYTES, ws_x + ((mt0 + tt) * KT + it) * A_BYTES, tile_bytes[tt],
@@ -269,21 +317,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++s == D) { s = 0; ph ^= 1u; }
       }
       for (int j = max(0, it - D); j < it; ++j)                  // copies in flight land before exit
-        if (!lbdev::mbar_wait(&full[j % D], (j / D) & 1)) ok = false;
+        if (!lbdev::mbar_wait(&full[j % D], (j / D) & 1, wait_ns)) ok = false;
     }
   } else if (warp == kWarpCodes) {
     // ---------------- code producer: 128 rows x 128 bytes per chunk, 128-byte swizzle
     if (lane == 0) {
       lbdev::prefetch_tmap(&tm_codes);
       int cc = 0;
-      for (; cc < NC; ++cc) {
+      for (; cc < NC && !test_fault; ++cc) {
         const int c = cc % CR;
-        if (!lbdev::mbar_wait(&c_empty[c], ((cc / CR) & 1) ^ 1)) { ok = false; break; }
+        if (!lbdev::mbar_wait(&c_empty[c], ((cc / CR) & 1) ^ 1, wait_ns)) { ok = false; break; }
         lbdev::mbar_arrive_expect_tx(&c_full[c], C_BYTES);
         lbdev::tma_load_2d(sC + c * C_BYTES, &tm_codes, 128 * cc, n0, &c_full[c]);
       }
       for (int j = max(0, cc - CR); j < cc; ++j)
-        if (!lbdev::mbar_wait(&c_full[j % CR], (j / CR) & 1)) ok = false;
+        if (!lbdev::mbar_wait(&c_full[j % CR], (j / CR) & 1, wait_ns)) ok = false;
     }
   } else if (warp == kWarpScales) {
     // ---------------- scale producer: 128 rows x 8 groups per chunk, [row][group] in shared memory
@@ -293,12 +341,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         int sc = 0;
         for (; sc < NS; ++sc) {
           const int c = sc % SR;
-          if (!lbdev::mbar_wait(&s_empty[c], ((sc / SR) & 1) ^ 1)) { ok = false; break; }
+          if (!lbdev::mbar_wait(&s_empty[c], ((sc / SR) & 1) ^ 1, wait_ns)) { ok = false; break; }
           lbdev::mbar_arrive_expect_tx(&s_full[c], S_BYTES);
           lbdev::tma_load_2d(sS + c * S_BYTES, &tm_scales, 8 * sc, n0, &s_full[c]);
         }
         for (int j = max(0, sc - SR); j < sc; ++j)
-          if (!lbdev::mbar_wait(&s_full[j % SR], (j / SR) & 1)) ok = false;
+          if (!lbdev::mbar_wait(&s_full[j % SR], (j / SR) & 1, wait_ns)) ok = false;
       }
     } else {
       // a scale row is not a multiple of 16 bytes: lane l loads rows l, l + 32, l + 64, l + 96 of
@@ -321,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       load(0);
       for (int sc = 0; sc < NS; ++sc) {
         const int c = sc % SR;
-        if (!lbdev::mbar_wait(&s_empty[c], ((sc / SR) & 1) ^ 1)) { ok = false; break; }
+        if (!lbdev::mbar_wait(&s_empty[c], ((sc / SR) & 1) ^ 1, wait_ns)) { ok = false; break; }
         uint8_t* dst = sS + c * S_BYTES;
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -345,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t bd = bdesc0;
       uint32_t acc_in = 0;
       for (int it = 0; it < KT; ++it) {
-        if (!lbdev::mbar_wait(&full[s], ph)) { ok = false; break; }
+        if (!lbdev::mbar_wait(&full[s], ph, wait_ns)) { ok = false; break; }
         lbdev::tc_fence_after();
         const uint32_t ad = tmem + static_cast<uint32_t>(32 * s);
         tc_mma_f16_ts(tmem + kAcc, ad, bd, idesc, acc_in);
@@ -376,8 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t ph = 0, cph = 0, sph = 0;
     int prev_s = -1;
     for (int it = par; it < KT && ok; it += 2) {
-      if (j < 2 && !lbdev::mbar_wait(&c_full[c], cph)) { ok = false; break; }
-      if (sj == 0 && !lbdev::mbar_wait(&s_full[cs], sph)) { ok = false; break; }
+      if (j < 2 && !lbdev::mbar_wait(&c_full[c], cph, wait_ns)) { ok = false; break; }
+      if (sj == 0 && !lbdev::mbar_wait(&s_full[cs], sph, wait_ns)) { ok = false; break; }
       // the chunk's 16-byte units are stored at unit ^ (row % 8) (128-byte swizzle)
       uint2 w;
       if (FMT == 1) {
@@ -411,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) lbdev::mbar_arrive(&full[prev_s]);
       }
-      if (!lbdev::mbar_wait(&empty[s], ph ^ 1)) { ok = false; break; }   // the slot's MMAs retired
+      if (!lbdev::mbar_wait(&empty[s], ph ^ 1, wait_ns)) { ok = false; break; }   // the slot's MMAs retired
       lbdev::tc_fence_after();
       tmem_st16(lane_base + static_cast<uint32_t>(32 * s + 16 * h), o);
       prev_s = s;
@@ -432,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) lbdev::mbar_arrive(&full[prev_s]);
     }
     // ---------------- epilogue: lane = weight row, columns = tokens; warp (h, par) takes 64 of them
-    if (!lbdev::mbar_wait(tmem_full, 0)) ok = false;
+    if (!lbdev::mbar_wait(tmem_full, 0, wait_ns)) ok = false;
     lbdev::tc_fence_after();
 #pragma unroll 1
     for (int c = 0; c < 2; ++c) {
@@ -445,11 +493,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
           const int tok = t0 + col + jj;
-          if (tok < m) {
-            const float f = __uint_as_float(v[jj]);
+          const float f = __uint_as_float(v[jj]) * sfac[col + jj];   // undo the prologue's 2^p
+          if (tok < m)
             y[static_cast<int64_t>(tok) * n + wrow] =
                 y_bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(f)) : __half_as_ushort(__float2half_rn(f));
-          }
         }
       }
     }
@@ -474,6 +521,7 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[LB_GEMM_NOALLOC_SCRAT
 namespace {
 std::mutex g_noalloc_mutex;
 void* g_noalloc_ptr[64] = {};
+unsigned long long g_noalloc_ctx[64] = {};
 }  // namespace
 
 namespace lb {
@@ -491,14 +539,17 @@ lb_status launch_gemm_noalloc(const lb_weight& W, const void* x, int xdt, int64_
   if (dev < 0 || dev >= 64) return fail(LB_ERR_UNSUPPORTED, "lb_gemm_noalloc: device index %d", dev);
   void* ptr = nullptr;
   {
-    // first call on this device (with it current): the host-side symbol is only a stand-in, the
-    // kernels need the array's device address
+    // set-up, once per device and context (with the device current): the host-side symbol is only
+    // a stand-in, the kernels need the array's device address; a new context (after a device
+    // reset) loads the module again, so the address is looked up again
+    const unsigned long long ctx = context_id();
     std::lock_guard<std::mutex> lk(g_noalloc_mutex);
-    if (!g_noalloc_ptr[dev]) {
+    if (!g_noalloc_ptr[dev] || ctx == 0 || ctx != g_noalloc_ctx[dev]) {
       void* p = nullptr;
       e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
       if (e != cudaSuccess) return cuda_fail(e, "lb_gemm_noalloc: cudaGetSymbolAddress");
       g_noalloc_ptr[dev] = p;
+      g_noalloc_ctx[dev] = ctx;
     }
     ptr = g_noalloc_ptr[dev];
   }
@@ -568,13 +619,16 @@ lb_status gemm_maps(const lb_weight& W, int scales_tma, CUtensorMap& tm_codes, C
 
 }  // namespace
 
+// Workspace: the binary16 activation tile images (mpad x k x 2 bytes), then one FP32 factor per
+// padded token row.
 size_t gemm_workspace_bytes(int64_t m, int64_t k) {
   const int64_t mpad = (m + BM - 1) / BM * BM;
-  return static_cast<size_t>(mpad) * static_cast<size_t>(k) * 2;
+  return static_cast<size_t>(mpad) * (static_cast<size_t>(k) * 2 + 4);
 }
 
 lb_status launch_gemm(const lb_weight& W, const void* x, int xdt, int64_t m, void* y, int ydt, void* ws,
                       cudaStream_t st) {
+  const bool fault = take_test_fault(kTestFaultGemm);
   uint32_t* err = device_error_word();
   if (!err) return fail(LB_ERR_CUDA, "lb_gemm: device error word unavailable");
   const int k = static_cast<int>(W.k), n = static_cast<int>(W.n);
@@ -584,16 +638,16 @@ lb_status launch_gemm(const lb_weight& W, const void* x, int xdt, int64_t m, voi
   CUtensorMap tm_codes, tm_scales;
   lb_status ms = gemm_maps(W, scales_tma, tm_codes, tm_scales);
   if (ms != LB_OK) return ms;
-  const int64_t total = mpad * (k / (one ? 32 : 16));               // one thread per K block of a row
-  const int64_t blocks = (total + 255) / 256;
   const uint16_t* xs = static_cast<const uint16_t*>(x);
   uint8_t* wsb = static_cast<uint8_t*>(ws);
+  float* fac = reinterpret_cast<float*>(wsb + static_cast<size_t>(mpad) * static_cast<size_t>(k) * 2);
+  const unsigned rows = static_cast<unsigned>(mpad);                // one CTA per (padded) token row
   if (xdt == LB_BF16) {
-    if (one) xprep_kernel<true, 1><<<static_cast<unsigned>(blocks), 256, 0, st>>>(xs, m, k, total, wsb, err);
-    else xprep_kernel<true, 2><<<static_cast<unsigned>(blocks), 256, 0, st>>>(xs, m, k, total, wsb, err);
+    if (one) xprep_kernel<true, 1><<<rows, 256, 0, st>>>(xs, m, k, wsb, fac);
+    else xprep_kernel<true, 2><<<rows, 256, 0, st>>>(xs, m, k, wsb, fac);
   } else {
-    if (one) xprep_kernel<false, 1><<<static_cast<unsigned>(blocks), 256, 0, st>>>(xs, m, k, total, wsb, err);
-    else xprep_kernel<false, 2><<<static_cast<unsigned>(blocks), 256, 0, st>>>(xs, m, k, total, wsb, err);
+    if (one) xprep_kernel<false, 1><<<rows, 256, 0, st>>>(xs, m, k, wsb, fac);
+    else xprep_kernel<false, 2><<<rows, 256, 0, st>>>(xs, m, k, wsb, fac);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "lb_gemm: prologue launch");
@@ -623,8 +677,10 @@ lb_status launch_gemm(const lb_weight& W, const void* x, int xdt, int64_t m, voi
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, one ? gemm_lowbit_kernel<1> : gemm_lowbit_kernel<2>, tm_codes, tm_scales,
-                         static_cast<const uint8_t*>(ws), W.scales, static_cast<uint16_t*>(y), static_cast<int>(m),
-                         static_cast<int>(mpad), n, k, scales_tma, ydt == LB_BF16 ? 1 : 0, err);
+                         static_cast<const uint8_t*>(ws), static_cast<const float*>(fac), W.scales,
+                         static_cast<uint16_t*>(y), static_cast<int>(m),
+                         static_cast<int>(mpad), n, k, scales_tma, ydt == LB_BF16 ? 1 : 0, err,
+                         fault ? kTestWaitNs : kWaitNs, fault ? 1 : 0);
   if (e != cudaSuccess) return cuda_fail(e, "lb_gemm: launch");
   return LB_OK;
 }

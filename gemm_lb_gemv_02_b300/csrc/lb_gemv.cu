@@ -15,15 +15,20 @@
 //     m (ternary: bits m, m+1) is copied from the code word has the exact value o + b, o = 2^(10-m),
 //     b the code bit (2-bit field).  One LOP3 (mask held in a register, exponent as immediate)
 //     builds two such halves, i.e. one half2 A-fragment register.
-//   * per group g and batch column c the constant C_g[c] = sum_k (o_k + h) x[c][k] (h = 1/2 for
-//     1-bit, 1 for ternary) is computed once per CTA in FP32 and fed as the MMA's C operand -C_g,
-//     so the tensor core returns sum_k (b_k - h) x_k: sum t x / 2 for 1-bit (t = 2b - 1) and
-//     sum t x for ternary (t = f - 1).  A values and products are exact.
+//   * 1-bit: per group g and batch column c the constant C_g[c] = sum_k (o_k + 1/2) x[c][k] is
+//     computed once per CTA in FP32 and fed as the MMA's C operand -C_g, so the tensor core
+//     returns sum_k (b_k - 1/2) x_k = sum t x / 2.  The offsets are kept <= 64, and every element
+//     of a 1-bit row counts in sum |s t x|, so the cancellation stays far inside the tolerance.
+//   * ternary: one HSUB2 turns o + f into f - 1 = t exactly, and the MMA starts from zero.  A zero
+//     code then contributes exactly nothing; a baseline would cancel o x against o x, and for a large
+//     x met by zero codes that rounding alone could exceed the tolerance of the row.
 //   * the group scale is applied once per group in FP32: acc += s * D_g; 1-bit doubles at the end.
 //   * the reduction order along K is free, so code bit j of a word lands in whichever k slot its
 //     register occupies; x is gathered once per CTA into B fragments in the matching order.
 //   * bfloat16 x is converted to binary16 after an exact power-of-two rescaling per batch column
-//     (undone on the FP32 result), so both activation types share the binary16 decode.
+//     that puts the column's largest magnitude in [2^15, 2^16) (undone on the FP32 result), so both
+//     activation types share the binary16 decode; every element within 2^32 of the column maximum
+//     is converted exactly.
 //
 // Memory pipeline: a producer warp streams the codes (and scales) of 128-row x 8-group tiles with
 // 2-D TMA loads (128-byte swizzled, so the consumers' fragment reads hit 32 distinct banks) into a
@@ -77,8 +82,10 @@ __host__ __device__ constexpr uint32_t expo16(int m) {   // 2^(10-m) in both hal
   return (static_cast<uint32_t>(25 - m) << 10) * 0x00010001u;
 }
 // 1-bit: register j of a 32-bit code word holds bits j (low half) and j+16 (high half) = weights
-// k = j and k = j + 16 of the word; mantissa position m_j in 1..9 (m >= 1 keeps o + 1/2 exact).
-__host__ __device__ constexpr int pos1(int j) { return j == 0 ? 1 : (j <= 9 ? j : j - 6); }
+// k = j and k = j + 16 of the word, at mantissa position m_j in 4..9: j = 0..5 from w << 4, j = 6..11
+// from w >> 2, j = 12..15 from w >> 8.  The offsets o = 2^(10-m) stay <= 64, so the baseline the
+// MMA cancels is at most 64.5 times the activations it multiplies (m >= 1 keeps o + 1/2 exact).
+__host__ __device__ constexpr int pos1(int j) { return j <= 5 ? j + 4 : (j <= 11 ? j - 2 : j - 8); }
 // Ternary: register p of a 32-bit word (16 fields) holds field p (low) and p + 8 (high) = weights
 // k = p and k = p + 8 of the word; the field sits at mantissa bits (m, m+1), m in {0,2,4,6,8}.
 __host__ __device__ constexpr int pos2(int p) { return p <= 4 ? 2 * p : 2 * p - 6; }
@@ -94,16 +101,21 @@ __device__ __forceinline__ uint32_t lop_and_or(uint32_t src, uint32_t mask) {   
   asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(src), "r"(mask), "n"(E));
   return r;
 }
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
 
-// Decoder state for one 32-bit code word: the word and its shifted copies.
+// Decoder state for one 32-bit code word: its shifted copies.
 struct Word1 {
-  uint32_t w, w1, w6;
+  uint32_t w4, w2, w8;
 };
-__device__ __forceinline__ Word1 prep1(uint32_t w) { return Word1{w, w << 1, w >> 6}; }
+__device__ __forceinline__ Word1 prep1(uint32_t w) { return Word1{w << 4, w >> 2, w >> 8}; }
 template <int J>
 __device__ __forceinline__ uint32_t dec1(const Word1& x, const uint32_t (&M)[10]) {
   constexpr int m = pos1(J);
-  const uint32_t src = J == 0 ? x.w1 : (J <= 9 ? x.w : x.w6);
+  const uint32_t src = J <= 5 ? x.w4 : (J <= 11 ? x.w2 : x.w8);
   return lop_and_or<expo16(m)>(src, M[m]);
 }
 struct Word2 {
@@ -117,11 +129,14 @@ __device__ __forceinline__ uint32_t dec2(const Word2& x, const uint32_t (&M)[10]
 }
 
 // A-fragment register I (0..15) of the lane's 32-k block of one row.
+//   1-bit: o + b; the MMA's C operand removes sum (o + 1/2) x, leaving sum t x / 2 (t = 2b - 1).
+//   ternary: (o + f) - (o + 1) = t exactly (SC[m] holds o + 1 in both halves), with no baseline:
+//   a zero code contributes exactly nothing, however large the activation it meets.
 template <int FMT, int I>
 __device__ __forceinline__ uint32_t areg(const Word1& a1, const Word2& a2lo, const Word2& a2hi,
-                                         const uint32_t (&M)[10]) {
+                                         const uint32_t (&M)[10], const uint32_t (&SC)[10]) {
   if constexpr (FMT == 1) return dec1<I>(a1, M);
-  else return dec2<(I & 7)>(I < 8 ? a2lo : a2hi, M);
+  else return hsub2(dec2<(I & 7)>(I < 8 ? a2lo : a2hi, M), SC[pos2(I & 7)]);
 }
 
 // D = A * B + C with C = {-C_g[2q], -C_g[2q+1], -C_g[2q], -C_g[2q+1]} (the baseline of my columns).
@@ -210,6 +225,10 @@ struct Args {
   int batch;
   int S;           // CTAs per cluster along K (chunk = cluster rank); 1 when count > 1
   int fuse;        // 1: SiLU-gated pair, p[0] = gate, p[1] = up (same n, k, x); h -> p[0].y
+  int shared;      // count > 1, S == 1, one x and one K for all: CTAs persistent over all units
+  int units;       // units of a shared launch
+  int test_fault;  // issue no weight copy, so that every pipeline wait gives up after wait_ns
+  uint64_t wait_ns;
 };
 
 template <int FMT, int BP>
@@ -246,11 +265,31 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   const int g_begin = static_cast<int>(rank) * gpc;
   const int ng = min(gpc, P.G - g_begin);                        // groups of this CTA's chunk (<= 0: none)
   const int nst = (ng + GS - 1) / GS;                            // stages per row block
-  // row blocks of this CTA: rb0, rb0 + rb_stride, ... (grouped launch: exactly one).  A fused
-  // SiLU-gated pair runs row block rb0 twice: unit 0 on the gate matrix, unit 1 on the up matrix.
+  // Units (row blocks) of this CTA, j = 0, 1, ...: one GEMV with persistent CTAs takes row blocks
+  // rb0, rb0 + gridDim.y, ...; a grouped launch whose problems share x and K (a.shared) takes units
+  // blockIdx.y, blockIdx.y + gridDim.y, ... of the whole unit list, whichever problem they belong
+  // to; any other grouped launch takes exactly its one unit; a fused SiLU-gated pair runs row
+  // block rb0 twice, unit 0 on the gate matrix and unit 1 on the up matrix.
   const int rb0 = static_cast<int>(blockIdx.y) - P.unit0;
-  const int rb_stride = a.fuse ? 0 : (a.count > 1 ? P.row_blocks : static_cast<int>(gridDim.y));
-  const int my_rbs = a.fuse ? 2 : (P.row_blocks - rb0 + rb_stride - 1) / rb_stride;
+  const int my_rbs = a.fuse ? 2
+                     : a.shared ? (a.units - static_cast<int>(blockIdx.y) + gridDim.y - 1) / gridDim.y
+                     : a.count > 1 ? 1
+                     : (P.row_blocks - rb0 + gridDim.y - 1) / gridDim.y;
+  auto unit_prob = [&](int j) -> int {
+    if (a.fuse) return j;
+    if (!a.shared) return pi;
+    const int u = static_cast<int>(blockIdx.y) + j * static_cast<int>(gridDim.y);
+    int q = 0;
+    for (int i = 1; i < a.count; ++i)
+      if (u >= a.p[i].unit0) q = i;
+    return q;
+  };
+  auto unit_rb = [&](int j) -> int {
+    if (a.fuse || (a.count > 1 && !a.shared)) return rb0;
+    if (!a.shared) return rb0 + j * static_cast<int>(gridDim.y);
+    const int u = static_cast<int>(blockIdx.y) + j * static_cast<int>(gridDim.y);
+    return u - a.p[unit_prob(j)].unit0;
+  };
   const int total_st = my_rbs * nst;
   bool ok = true;
 
@@ -267,18 +306,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   if (warp == NW) {
     // ======================= producer: weights do not depend on earlier kernels, so no wait
     if (lane == 0) {
-      lbdev::prefetch_tmap(&P.tm_codes);
-      if (P.scales_tma) lbdev::prefetch_tmap(&P.tm_scales);
-      if (a.fuse) {
-        lbdev::prefetch_tmap(&a.p[1].tm_codes);
-        if (P.scales_tma) lbdev::prefetch_tmap(&a.p[1].tm_scales);
-      }
+      for (int i = 0; i < a.count; ++i)
+        if (i == pi || a.fuse || a.shared) {
+          lbdev::prefetch_tmap(&a.p[i].tm_codes);
+          if (P.scales_tma) lbdev::prefetch_tmap(&a.p[i].tm_scales);
+        }
       const uint32_t bytes = static_cast<uint32_t>(FT::nb * kBox + (P.scales_tma ? kScaleBox : 0));
-      for (int st = 0; st < total_st; ++st) {
+      for (int st = 0; st < total_st && !a.test_fault; ++st) {
         const int s = st % L::stages;
-        if (!lbdev::mbar_wait(&empty[s], static_cast<uint32_t>(((st / L::stages) & 1) ^ 1))) { ok = false; break; }
-        const int row0 = (rb0 + (st / nst) * rb_stride) * ROWS;
-        const Prob& PU = a.p[a.fuse ? st / nst : pi];              // the matrix of this unit
+        if (!lbdev::mbar_wait(&empty[s], static_cast<uint32_t>(((st / L::stages) & 1) ^ 1), a.wait_ns)) {
+          ok = false;
+          break;
+        }
+        const int row0 = unit_rb(st / nst) * ROWS;
+        const Prob& PU = a.p[unit_prob(st / nst)];                 // the matrix of this unit
         const int g0 = g_begin + (st % nst) * GS;
         uint8_t* slot = sm + s * L::slot;
         lbdev::mbar_arrive_expect_tx(&full[s], bytes);
@@ -300,7 +341,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     griddep_wait();                                   // x is read and y written only after this
 
     // ---- x prologue.  Tuple (g, n, qq): the 32 activations x[n][128(g_begin+g) + 32qq ..] of one
-    // fragment lane.  bfloat16: first the per-column maximum over the chunk, then an exact 2^p.
+    // fragment lane.  bfloat16 columns are scaled by an exact power of two 2^p that puts the
+    // column's largest magnitude in [2^15, 2^16) (|p| <= 126) and converted to binary16: every
+    // element within 2^32 of the column maximum is then exact (8 significant bits fit binary16 down
+    // to 2^-17), smaller ones round to the binary16 subnormal grid, nothing overflows, and the FP32
+    // result is scaled back by 2^-p.  A thread's first tuple stays in registers between the two
+    // passes, so the common case reads x from memory once.
     const int tuples = ng * BP * 4;
     auto load32 = [&](int t, uint32_t (&X)[16]) -> bool {
       const int qq = t & 3, n = (t >> 2) % BP, g = (t >> 2) / BP;
@@ -318,45 +364,46 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
       }
       return true;
     };
+    uint32_t X0[16];
+    const bool act0 = load32(static_cast<int>(threadIdx.x), X0);
     if (XBF) {
       uint32_t* cmax = reinterpret_cast<uint32_t*>(colf + 8);
-      for (int base = 0; base < tuples; base += NW * 32) {
+      uint32_t mx = 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) mx = max(mx, max((X0[i] << 16) & 0x7f800000u, X0[i] & 0x7f800000u));
+      if (act0) atomicMax(&cmax[(threadIdx.x >> 2) % BP], mx);      // exponent fields order like magnitudes
+      for (int base = NW * 32; base < tuples; base += NW * 32) {
         const int t = base + static_cast<int>(threadIdx.x);
         uint32_t X[16];
         if (load32(t, X)) {
-          uint32_t mx = 0;
+          mx = 0;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) mx = max(mx, max((X[i] << 16) & 0x7fffffffu, X[i] & 0x7fff0000u));
-          atomicMax(&cmax[(t >> 2) % BP], mx);          // IEEE bit patterns of |x| order like values
+          for (int i = 0; i < 16; ++i) mx = max(mx, max((X[i] << 16) & 0x7f800000u, X[i] & 0x7f800000u));
+          atomicMax(&cmax[(t >> 2) % BP], mx);
         }
       }
       consumer_sync();
     }
-    if (threadIdx.x < 8) {
-      float f = 1.f;
-      if (XBF) {
-        const uint32_t mx = reinterpret_cast<uint32_t*>(colf + 8)[threadIdx.x];
-        if (mx != 0u) {
-          const int e = static_cast<int>((mx >> 23) & 0xFF);
-          const int p = max(-126, min(126, 127 - e));                         // max * 2^p in [1, 2)
-          f = __uint_as_float(static_cast<uint32_t>(127 - p) << 23);          // 2^-p
-        }
-      }
-      colf[threadIdx.x] = f;
-    }
+    auto col_p = [&](int n) -> int {                               // the column's exponent p
+      const int e = static_cast<int>(reinterpret_cast<uint32_t*>(colf + 8)[n] >> 23) - 127;   // -127: zero
+      return max(-126, min(126, 15 - e));
+    };
+    if (threadIdx.x < 8)                                           // 2^-p (1 for binary16 columns)
+      colf[threadIdx.x] = XBF ? __uint_as_float(static_cast<uint32_t>(127 - col_p(threadIdx.x)) << 23) : 1.f;
     for (int base = 0; base < tuples; base += NW * 32) {          // uniform: quads stay together
       const int t = base + static_cast<int>(threadIdx.x);
       const int qq = t & 3, n = (t >> 2) % BP, g = (t >> 2) / BP;
       uint32_t X[16];
-      const bool act = load32(t, X);
+      bool act;
+      if (base == 0) {
+        act = act0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) X[i] = X0[i];
+      } else {
+        act = load32(t, X);
+      }
       if (XBF && act) {
-        const uint32_t mx = reinterpret_cast<uint32_t*>(colf + 8)[n];
-        float scale = 1.f;
-        if (mx != 0u) {
-          const int e = static_cast<int>((mx >> 23) & 0xFF);
-          const int p = max(-126, min(126, 127 - e));
-          scale = __uint_as_float(static_cast<uint32_t>(127 + p) << 23);      // 2^p (exact)
-        }
+        const float scale = __uint_as_float(static_cast<uint32_t>(127 + col_p(n)) << 23);   // 2^p (exact)
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float lo = __uint_as_float(X[i] << 16) * scale, hi = __uint_as_float(X[i] & 0xffff0000u) * scale;
@@ -365,7 +412,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         }
       }
       uint32_t B[16];
-      float c = 0.f;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         uint32_t lo_src, hi_src, sel;
@@ -376,25 +422,40 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
           lo_src = X[8 * uu + (p >> 1)]; hi_src = X[8 * uu + (p >> 1) + 4]; sel = (p & 1) ? 0x7632 : 0x5410;
         }
         B[i] = __byte_perm(lo_src, hi_src, sel);
-        const float2 fv = __half22float2(*reinterpret_cast<const __half2*>(&B[i]));
-        c = fmaf(reg_offset<FMT>(i) + FT::h, fv.x + fv.y, c);
       }
-      c += __shfl_xor_sync(0xffffffffu, c, 1);
-      c += __shfl_xor_sync(0xffffffffu, c, 2);
+      float c = 0.f;
+      if (FMT == 1) {
+        // 1-bit baseline sum_k (o_k + 1/2) x_k: the activations of each offset are summed first
+        // (no large multiplier inside), then one product per offset
+#pragma unroll
+        for (int m = 4; m <= 9; ++m) {
+          float sx = 0.f;
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (pos1(i) == m) {
+              const float2 fv = __half22float2(*reinterpret_cast<const __half2*>(&B[i]));
+              sx += fv.x + fv.y;
+            }
+          c = fmaf(static_cast<float>(1 << (10 - m)) + 0.5f, sx, c);
+        }
+        c += __shfl_xor_sync(0xffffffffu, c, 1);
+        c += __shfl_xor_sync(0xffffffffu, c, 2);
+      }
       if (t < tuples) {
         uint8_t* dst = xs + g * L::xgroup + (n * 4 + qq) * 16;
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           *reinterpret_cast<uint4*>(dst + i * (L::xgroup / 4)) = make_uint4(B[4 * i], B[4 * i + 1], B[4 * i + 2], B[4 * i + 3]);
-        if (qq == 0) {
+        if (FMT == 1 && qq == 0) {
           const float v = act ? -c : 0.f;
           cneg[g * 16 + (n >> 1) * 4 + (n & 1)] = v;
           cneg[g * 16 + (n >> 1) * 4 + 2 + (n & 1)] = v;
         }
       }
     }
-    for (int i = threadIdx.x; i < ng * 16; i += NW * 32) {          // columns beyond the padded batch
-      if (((i >> 2) & 3) * 2 + (i & 1) >= BP) cneg[i] = 0.f;
+    if (FMT == 1) {
+      for (int i = threadIdx.x; i < ng * 16; i += NW * 32)          // columns beyond the padded batch
+        if (((i >> 2) & 3) * 2 + (i & 1) >= BP) cneg[i] = 0.f;
     }
     consumer_sync();
 
@@ -404,7 +465,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     // ---- per-thread constants
     uint32_t M[10];                                    // decode masks, kept in registers
     constexpr uint32_t kMask = FMT == 1 ? 0x00010001u : 0x00030003u;
-#define LB_MASK(m) asm volatile("mov.b32 %0, %1;" : "=r"(M[m]) : "n"(kMask << (m)))
+    uint32_t SC[10];                                   // ternary: o + 1 in both halves, by position
+#define LB_MASK(m)                                                                                   \
+  asm volatile("mov.b32 %0, %1;" : "=r"(M[m]) : "n"(kMask << (m)));                                 \
+  asm volatile("mov.b32 %0, %1;" : "=r"(SC[m]) : "n"(expo16(m) | (0x00010001u << (m))))
     LB_MASK(0); LB_MASK(1); LB_MASK(2); LB_MASK(3); LB_MASK(4);
     LB_MASK(5); LB_MASK(6); LB_MASK(7); LB_MASK(8); LB_MASK(9);
 #undef LB_MASK
@@ -430,25 +494,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     uint32_t ph = 0;
 
     for (int st = 0; st < total_st; ++st) {
-      const int rb = rb0 + i_rb * rb_stride;
+      const int rb = unit_rb(i_rb);
+      const Prob& PU = a.p[unit_prob(i_rb)];                      // the matrix of this unit
       const int g0 = cstage * GS + half * GH;                     // my first group, relative to g_begin
       const int cnt = min(GH, ng - g0);                           // my groups in this stage (may be <= 0)
       const uint32_t slot = sm32 + static_cast<uint32_t>(s * L::slot);
       float sa[GH], sb[GH];
       if (!P.scales_tma) {                                        // fallback: scales from L2
-        const Prob& PU = a.p[a.fuse ? i_rb : pi];
         const int row_a = rb * ROWS + ia, row_b = row_a + 8;
 #pragma unroll
         for (int j = 0; j < GH; ++j) {
           sa[j] = 0.f; sb[j] = 0.f;
           if (j < cnt) {
             const int64_t g = g_begin + g0 + j;
-            if (row_a < P.n) sa[j] = __half2float(__ushort_as_half(__ldg(PU.scales + static_cast<int64_t>(row_a) * P.G + g)));
-            if (row_b < P.n) sb[j] = __half2float(__ushort_as_half(__ldg(PU.scales + static_cast<int64_t>(row_b) * P.G + g)));
+            if (row_a < PU.n) sa[j] = __half2float(__ushort_as_half(__ldg(PU.scales + static_cast<int64_t>(row_a) * PU.G + g)));
+            if (row_b < PU.n) sb[j] = __half2float(__ushort_as_half(__ldg(PU.scales + static_cast<int64_t>(row_b) * PU.G + g)));
           }
         }
       }
-      if (ok && !lbdev::mbar_wait(&full[s], ph)) ok = false;
+      if (ok && !lbdev::mbar_wait(&full[s], ph, a.wait_ns)) ok = false;
       ok = __all_sync(0xffffffffu, ok);
       // ---- the stage's codes and scales -> registers, then the slot goes back to the producer
       uint2 ca[GH], cb[GH];                                        // rows ia / ia + 8, my 4 groups
@@ -486,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         auto one_group = [&](int j) {
           Word1 w1a = prep1(ca[j].x), w1b = prep1(cb[j].x);
           Word2 wla = prep2(ca[j].x), wha = prep2(ca[j].y), wlb = prep2(cb[j].x), whb = prep2(cb[j].y);
-          const float4 cn = lds128f(cbase + j * 64);
+          const float4 cn = FMT == 1 ? lds128f(cbase + j * 64) : make_float4(0.f, 0.f, 0.f, 0.f);
           uint4 bx[4];
 #pragma unroll
           for (int iq = 0; iq < 4; ++iq) bx[iq] = lds128(xbase + j * L::xgroup + iq * (L::xgroup / 4));
@@ -495,8 +559,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   {                                                                                                        \
     const uint32_t blo = (I) % 2 == 0 ? bx[(I) / 2].x : bx[(I) / 2].z;                                      \
     const uint32_t bhi = (I) % 2 == 0 ? bx[(I) / 2].y : bx[(I) / 2].w;                                      \
-    const uint32_t e0 = areg<FMT, 2 * (I)>(w1a, wla, wha, M), e1 = areg<FMT, 2 * (I)>(w1b, wlb, whb, M);      \
-    const uint32_t e2 = areg<FMT, 2 * (I) + 1>(w1a, wla, wha, M), e3 = areg<FMT, 2 * (I) + 1>(w1b, wlb, whb, M); \
+    const uint32_t e0 = areg<FMT, 2 * (I)>(w1a, wla, wha, M, SC), e1 = areg<FMT, 2 * (I)>(w1b, wlb, whb, M, SC);      \
+    const uint32_t e2 = areg<FMT, 2 * (I) + 1>(w1a, wla, wha, M, SC), e3 = areg<FMT, 2 * (I) + 1>(w1b, wlb, whb, M, SC); \
     if ((I) == 0) mma_c4(d, e0, e1, e2, e3, blo, bhi, cn);                                                 \
     else mma_acc(d, e0, e1, e2, e3, blo, bhi);                                                             \
   }
@@ -514,7 +578,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             Word1 w1a0 = prep1(ca[jp].x), w1b0 = prep1(cb[jp].x), w1a1 = prep1(ca[jp + 1].x), w1b1 = prep1(cb[jp + 1].x);
             Word2 la0 = prep2(ca[jp].x), ha0 = prep2(ca[jp].y), lb0 = prep2(cb[jp].x), hb0 = prep2(cb[jp].y);
             Word2 la1 = prep2(ca[jp + 1].x), ha1 = prep2(ca[jp + 1].y), lb1 = prep2(cb[jp + 1].x), hb1 = prep2(cb[jp + 1].y);
-            const float4 cn0 = lds128f(cbase + jp * 64), cn1 = lds128f(cbase + (jp + 1) * 64);
+            const float4 cn0 = FMT == 1 ? lds128f(cbase + jp * 64) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 cn1 = FMT == 1 ? lds128f(cbase + (jp + 1) * 64) : make_float4(0.f, 0.f, 0.f, 0.f);
             uint4 bx0[4], bx1[4];
 #pragma unroll
             for (int iq = 0; iq < 4; ++iq) {
@@ -528,12 +593,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     const uint32_t b0hi = (I) % 2 == 0 ? bx0[(I) / 2].y : bx0[(I) / 2].w;                                   \
     const uint32_t b1lo = (I) % 2 == 0 ? bx1[(I) / 2].x : bx1[(I) / 2].z;                                   \
     const uint32_t b1hi = (I) % 2 == 0 ? bx1[(I) / 2].y : bx1[(I) / 2].w;                                   \
-    const uint32_t e00 = areg<FMT, 2 * (I)>(w1a0, la0, ha0, M), e01 = areg<FMT, 2 * (I)>(w1b0, lb0, hb0, M);  \
-    const uint32_t e02 = areg<FMT, 2 * (I) + 1>(w1a0, la0, ha0, M);                                         \
-    const uint32_t e03 = areg<FMT, 2 * (I) + 1>(w1b0, lb0, hb0, M);                                         \
-    const uint32_t e10 = areg<FMT, 2 * (I)>(w1a1, la1, ha1, M), e11 = areg<FMT, 2 * (I)>(w1b1, lb1, hb1, M);  \
-    const uint32_t e12 = areg<FMT, 2 * (I) + 1>(w1a1, la1, ha1, M);                                         \
-    const uint32_t e13 = areg<FMT, 2 * (I) + 1>(w1b1, lb1, hb1, M);                                         \
+    const uint32_t e00 = areg<FMT, 2 * (I)>(w1a0, la0, ha0, M, SC), e01 = areg<FMT, 2 * (I)>(w1b0, lb0, hb0, M, SC);  \
+    const uint32_t e02 = areg<FMT, 2 * (I) + 1>(w1a0, la0, ha0, M, SC);                                         \
+    const uint32_t e03 = areg<FMT, 2 * (I) + 1>(w1b0, lb0, hb0, M, SC);                                         \
+    const uint32_t e10 = areg<FMT, 2 * (I)>(w1a1, la1, ha1, M, SC), e11 = areg<FMT, 2 * (I)>(w1b1, lb1, hb1, M, SC);  \
+    const uint32_t e12 = areg<FMT, 2 * (I) + 1>(w1a1, la1, ha1, M, SC);                                         \
+    const uint32_t e13 = areg<FMT, 2 * (I) + 1>(w1b1, lb1, hb1, M, SC);                                         \
     if ((I) == 0) {                                                                                        \
       mma_c4(d0, e00, e01, e02, e03, b0lo, b0hi, cn0);                                                     \
       mma_c4(d1, e10, e11, e12, e13, b1lo, b1hi, cn1);                                                     \
@@ -582,8 +647,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
           } else if (a.S == 1) {
             const int row_a = rb * ROWS + ia, row_b = row_a + 8;
             auto put = [&](int row, int col, float v) {
-              if (row < P.n && col < a.batch)
-                P.y[static_cast<int64_t>(col) * P.n + row] =
+              if (row < PU.n && col < a.batch)
+                PU.y[static_cast<int64_t>(col) * PU.n + row] =
                     XBF ? __bfloat16_as_ushort(__float2bfloat16_rn(v)) : __half_as_ushort(__float2half_rn(v));
             };
             put(row_a, c0col, a.fuse ? silu(gate[0]) * v0 : v0);
@@ -753,6 +818,8 @@ lb_status fill_prob(const lb_weight& W, const void* x, void* y, int gpc, Prob& p
 
 template <int FMT, bool XBF, int BP>
 lb_status launch_args(Args& args, int grid_x, int grid_y, int smem, cudaStream_t st) {
+  args.test_fault = lb::take_test_fault(lb::kTestFaultGemv) ? 1 : 0;
+  args.wait_ns = args.test_fault ? lb::kTestWaitNs : lb::kWaitNs;
   args.err = lb::device_error_word();
   if (!args.err) return lb::fail(LB_ERR_CUDA, "lb_gemv: device error word unavailable");
   {
@@ -867,6 +934,16 @@ lb_status launch_many(const lb_gemv_problem* probs, int count, int batch, cudaSt
   args.count = count;
   args.batch = batch;
   args.S = best_s;
+  // one x and one K for every problem (q / k / v, gate / up): persistent CTAs over all the units,
+  // one x prologue per CTA
+  bool same = best_s == 1;
+  for (int i = 1; i < count; ++i)
+    same = same && probs[i].x == probs[0].x && probs[i].W.k == probs[0].W.k;
+  if (same && count > 1) {
+    args.shared = 1;
+    args.units = units;
+    return launch_args<FMT, XBF, BP>(args, 1, min(units, sms), smem, st);
+  }
   return launch_args<FMT, XBF, BP>(args, best_s, units, smem, st);
 }
 

@@ -31,8 +31,9 @@ STATUS_NAMES = {0: "LB_OK", 1: "LB_ERR_NULL", 2: "LB_ERR_SHAPE", 3: "LB_ERR_ALIG
 # Symbols declared in include/lb.h (checked by the tests against the header and the library).
 EXPORTED = ("lb_status_string", "lb_last_error", "lb_version", "lb_packed_bytes", "lb_pack_1bit",
             "lb_pack_ternary", "lb_gemv", "lb_gemm_workspace_bytes", "lb_gemm", "lb_device_error",
-            "lb_gemm_noalloc", "lb_gemv_batched", "lb_embed", "lb_gemv_swiglu", "lb_pack_ternary5")
-LB_GEMM_NOALLOC_SCRATCH_BYTES = 8 << 20
+            "lb_gemm_noalloc", "lb_gemv_batched", "lb_embed", "lb_gemv_swiglu", "lb_pack_ternary5",
+            "lb_read_probe")
+LB_GEMM_NOALLOC_SCRATCH_BYTES = (8 << 20) + (64 << 10)
 LB_GEMV_BATCH_MAX = 8
 
 
@@ -75,6 +76,7 @@ def _load():
         "lb_gemv_batched": ([ctypes.POINTER(lb_gemv_problem), i32, i32, i32, vp], i32),
         "lb_embed": ([ctypes.POINTER(lb_weight), vp, i64, vp, i32, vp], i32),
         "lb_gemv_swiglu": ([ctypes.POINTER(lb_weight), ctypes.POINTER(lb_weight), vp, i32, i32, vp, vp], i32),
+        "lb_read_probe": ([vp, ctypes.c_size_t, vp, vp], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -200,6 +202,11 @@ def lb_gemv_swiglu(Wg: lb_weight, Wu: lb_weight, x, xdt: int, batch: int, h, str
 def lb_embed(W: lb_weight, ids, count: int, out, out_dtype: int, stream=None) -> None:
     """Embedding rows out[i] = dequantised row ids[i] of W (ids: int32 device tensor)."""
     _check(_lib.lb_embed(ctypes.byref(W), _ptr(ids), count, _ptr(out), out_dtype, _stream(stream)), "lb_embed")
+
+
+def lb_read_probe(data, nbytes: int, sink, stream=None) -> None:
+    """Read nbytes of device memory (the read-bandwidth reference of one launch); sink: uint32."""
+    _check(_lib.lb_read_probe(_ptr(data), nbytes, _ptr(sink), _stream(stream)), "lb_read_probe")
 
 
 def lb_device_error(clear: bool = False) -> int:

@@ -128,3 +128,45 @@ def matrix_inputs(w: Workload, index: int):
 def workload_activations(w: Workload, index: int, batch: int) -> torch.Tensor:
     m = w.matrices[index]
     return activations(batch, m.k, w.xdtype, matrix_seed(w, index, 2 + batch))
+
+
+def activations_wide_range(b: int, k: int, dtype: str, seed: int) -> torch.Tensor:
+    """Activation rows that stress the numeric range of the 16-bit inputs, shape [b][k] (b >= 5).
+
+    bfloat16 rows: 0 N(0,1) scaled so that max |x| = 3e38 (near the largest finite bfloat16);
+    1 N(0,1) * 1e30; 2 N(0,1) * 1e5; 3 N(0,1) * 1e-4 with one element of magnitude ~1e4 per 128
+    (ratio 1e8 inside a group); 4 all zeros (+0), 5 N(0,1) * 1e-4 with one ~1e4 element in the
+    whole row, 6 N(0,1) with +-0 in every fourth position, 7 N(0,1) * 2^-120 (tiny normals).
+    binary16 rows: 0 N(0,1) with one element of magnitude ~6e4 per 128; 1 subnormals
+    (N(0,1) * 2^-20); 2 N(0,1) * 1e-3 with a few elements ~3e4; 3 N(0,1); 4 all zeros (+0);
+    5 N(0,1) with +-0 in every fourth position; 6 N(0,1) * 100; 7 N(0,1) * 2^-14.
+    Rows beyond b are dropped; rows are chosen by index modulo 8.
+    """
+    g = _gen(seed)
+    z = torch.randn(8, k, generator=g, dtype=torch.float64)
+    u = torch.rand(8, k, generator=g, dtype=torch.float64)
+    pos_group = (torch.arange(k) % GROUP) == (seed % GROUP)
+    one_pos = torch.arange(k) == ((seed * 7919) % k)
+    rows = torch.zeros(8, k, dtype=torch.float64)
+    if dtype == "bf16":
+        rows[0] = z[0] / z[0].abs().max() * 3e38
+        rows[1] = z[1] * 1e30
+        rows[2] = z[2] * 1e5
+        rows[3] = torch.where(pos_group, torch.sign(z[3]) * (1e4 + 1e3 * u[3]), z[3] * 1e-4)
+        rows[4] = 0.0
+        rows[5] = torch.where(one_pos, torch.sign(z[5]) * (1e4 + 1e3 * u[5]), z[5] * 1e-4)
+        rows[6] = torch.where(torch.arange(k) % 4 == 0, torch.where(u[6] < 0.5, 0.0, -0.0), z[6])
+        rows[7] = z[7] * 2.0 ** -120
+        tdt = torch.bfloat16
+    else:
+        rows[0] = torch.where(pos_group, torch.sign(z[0]) * (5e4 + 1e4 * u[0]), z[0])
+        rows[1] = z[1] * 2.0 ** -20
+        rows[2] = torch.where(torch.arange(k) % 509 == 3, torch.sign(z[2]) * 3e4, z[2] * 1e-3)
+        rows[3] = z[3]
+        rows[4] = 0.0
+        rows[5] = torch.where(torch.arange(k) % 4 == 0, torch.where(u[5] < 0.5, 0.0, -0.0), z[5])
+        rows[6] = z[6] * 100.0
+        rows[7] = z[7] * 2.0 ** -14
+        tdt = torch.float16
+    idx = torch.arange(b) % 8
+    return rows[idx].to(torch.float32).to(tdt)

@@ -150,8 +150,8 @@ lb_status lb_pack_ternary5(const int8_t* t, const uint16_t* s_in, int64_t n, int
  * batch : 1 .. 8.
  * Asynchronous on `stream`.  Errors (no launch): LB_ERR_NULL, LB_ERR_SHAPE, LB_ERR_ALIGN,
  * LB_ERR_DTYPE; LB_ERR_UNSUPPORTED if k is longer than 8 CTAs of a cluster hold in shared memory
- * (k <= 352256 at batch 1, 196608 at batch 2, 98304 at batch 3-4, 49152 at batch 5-8);
- * LB_ERR_CUDA if the launch fails.
+ * (1-bit: k <= 352256 at batch 1, 196608 at batch 2, 98304 at batch 3-4, 49152 at batch 5-8;
+ * ternary: k <= 376832, 204800, 106496, 49152); LB_ERR_CUDA if the launch fails.
  */
 lb_status lb_gemv(const lb_weight* W, const void* x, int xdt, int batch, void* y, lb_stream stream);
 
@@ -215,15 +215,18 @@ lb_status lb_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k, int xdt, size
  * FP32 accumulation on the tensor cores, output rounded to `ydt` (RNE).
  *
  * W                : packed matrix (n x k), 1-bit or ternary; n must be a multiple of 16.
- * x                : device [m][k] of `xdt`, 16-byte aligned.  Values must lie in the binary16
- *                    range |x| <= 65504 (the product runs on FP16 tensor-core operands, where
- *                    s * t is exact); bfloat16 inputs are converted to binary16 first.
+ * x                : device [m][k] of `xdt`, 16-byte aligned, any finite values.  The product runs
+ *                    on FP16 tensor-core operands, where s * t is exact.  binary16 rows are used as
+ *                    they are; each bfloat16 row is first scaled by an exact power of two that puts
+ *                    its largest magnitude in [2^15, 2^16), converted to binary16 (exact for every
+ *                    element within 2^32 of the row maximum; smaller ones round to the binary16
+ *                    subnormal grid), and the FP32 results are scaled back.
  * y                : device [m][n] of `ydt`, 16-byte aligned.
  * workspace        : device scratch of at least lb_gemm_workspace_bytes(...) bytes, 256-byte
  *                    aligned, used only during this call's kernels (may be reused afterwards).
  * Asynchronous on `stream`.  Errors (no launch): LB_ERR_NULL, LB_ERR_SHAPE, LB_ERR_ALIGN,
- * LB_ERR_DTYPE, LB_ERR_WORKSPACE; LB_ERR_CUDA.  Limits of one call: 1 <= m <= 65535 * 256 and
- * ceil(m / 128) * 128 * k <= (2^31 - 1) * 4096 (LB_ERR_SHAPE beyond).  Any m is served by the
+ * LB_ERR_DTYPE, LB_ERR_WORKSPACE; LB_ERR_CUDA.  Limit of one call: 1 <= m <= 65535 * 256
+ * (LB_ERR_SHAPE beyond).  Any m is served by the
  * same kernels: a token tile holding fewer than 256 tokens runs its tensor-core products only as
  * wide as its token count (rounded up to 16), so mid-size m (16 .. 128) pays for the tokens it
  * has.
@@ -256,13 +259,14 @@ lb_status lb_embed(const lb_weight* W, const int32_t* ids, int64_t count, void* 
  * Sticky device-side error word of the current device (0 = none).  Kernels that wait on an
  * mbarrier give up after a bounded number of polls, set a bit here and return instead of
  * hanging.  lb_device_error() synchronises the device, reads the word and, if `clear` is
- * non-zero, resets it.  Bit 0: a GEMM pipeline wait timed out.  Bit 1: a GEMM activation lay
- * outside the binary16 range.  Bit 2: an lb_embed row id lay outside [0, n).
+ * non-zero, resets it.  Bit 0: a GEMM or GEMV pipeline wait timed out.  Bit 1: unused.  Bit 2:
+ * an lb_embed row id lay outside [0, n).
  */
 lb_status lb_device_error(uint32_t* word, int clear);
 
-/* Size of the library-owned scratch used by lb_gemm_noalloc (8 MiB). */
-#define LB_GEMM_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+/* Size of the library-owned scratch used by lb_gemm_noalloc: 8 MiB of activation tiles plus 64 KiB
+ * of per-token factors, e.g. 512 tokens at k = 8192. */
+#define LB_GEMM_NOALLOC_SCRATCH_BYTES (((size_t)8 << 20) + ((size_t)64 << 10))
 
 /*
  * lb_gemm without a caller-provided workspace and without any allocation.  (The pages describe
@@ -289,6 +293,19 @@ lb_status lb_device_error(uint32_t* word, int clear);
  */
 lb_status lb_gemm_noalloc(const lb_weight* W, const void* x, int xdt, int64_t m, void* y, int ydt,
                           lb_stream stream);
+
+/*
+ * Read-bandwidth reference (no part of the method; the pages describe no such call): reads `bytes`
+ * bytes of device memory with plain 16-byte loads in one launch shaped like the decode GEMV's (every
+ * CTA lets the next kernel on the stream launch at once), and XORs all it read into *sink, so that
+ * the benchmark can time the practical read ceiling of one launch of a GEMV's byte count.
+ *
+ * data  : device buffer, 16-byte aligned, read only.   bytes : a multiple of 16 (0 launches nothing).
+ * sink  : device uint32, 4-byte aligned; its value is a checksum of no meaning.
+ * Asynchronous on `stream`.  Errors (no launch): LB_ERR_NULL, LB_ERR_ALIGN, LB_ERR_SHAPE (bytes not
+ * a multiple of 16); LB_ERR_CUDA if the launch fails.
+ */
+lb_status lb_read_probe(const void* data, size_t bytes, uint32_t* sink, lb_stream stream);
 
 #ifdef __cplusplus
 }

@@ -54,6 +54,10 @@ def _status(fn, *args):
     return "LB_OK"
 
 
+# The largest k lb_gemv takes per batch class (batch 1, 2, 3-4, 5-8), as include/lb.h states them.
+GEMV_K_LIMITS = {lb.LB_FMT_1BIT_G128: ((1, 352256), (2, 196608), (4, 98304), (8, 49152)),
+                 lb.LB_FMT_TERNARY_G128: ((1, 376832), (2, 204800), (4, 106496), (8, 49152))}
+
 # Fake, never-dereferenced device addresses: validation must reject before any CUDA call.
 A16 = 0x10000
 MIS = 0x10001
@@ -85,7 +89,7 @@ def test_gemv_validation():
 def test_gemm_validation():
     W = lb.make_weight(lb.LB_FMT_TERNARY_G128, 256, 256, A16, A16)
     need = lb.lb_gemm_workspace_bytes(5, 256, 256, lb.LB_BF16)
-    assert need == 128 * 256 * 2
+    assert need == 128 * (256 * 2 + 4)                   # binary16 tiles + one FP32 factor per padded row
     assert _status(lb.lb_gemm, W, A16, lb.LB_BF16, 5, A16, lb.LB_BF16, None, 0, 0) == "LB_ERR_WORKSPACE"
     assert _status(lb.lb_gemm, W, A16, lb.LB_BF16, 5, A16, lb.LB_BF16, A16, need - 1, 0) == "LB_ERR_WORKSPACE"
     assert _status(lb.lb_gemm, W, A16, lb.LB_BF16, 5, A16, lb.LB_BF16, A16 + 16, need, 0) == "LB_ERR_ALIGN"
@@ -95,12 +99,12 @@ def test_gemm_validation():
     assert _status(lb.lb_gemm, lb.make_weight(1, 250, 256, A16, A16), A16, lb.LB_BF16, 5, A16, lb.LB_BF16,
                    A16, need, 0) == "LB_ERR_SHAPE"
     assert _status(lb.lb_gemm, W, A16, 5, 5, A16, lb.LB_BF16, A16, need, 0) == "LB_ERR_DTYPE"
-    # launch-shape limits: 65535 token tiles of 256; the activation prologue's grid
+    # launch-shape limit: 65535 token tiles of 256; beyond it only the workspace bounds a call
     W128 = lb.make_weight(lb.LB_FMT_TERNARY_G128, 256, 128, A16, A16)
     assert _status(lb.lb_gemm, W128, A16, lb.LB_BF16, 65535 * 256 + 1, A16, lb.LB_BF16, A16, need, 0) == "LB_ERR_SHAPE"
     assert _status(lb.lb_gemm, W128, A16, lb.LB_BF16, 65535 * 256, A16, lb.LB_BF16, A16, need, 0) == "LB_ERR_WORKSPACE"
     Wk = lb.make_weight(lb.LB_FMT_TERNARY_G128, 256, 1 << 24, A16, A16)
-    assert _status(lb.lb_gemm, Wk, A16, lb.LB_BF16, 1 << 20, A16, lb.LB_BF16, A16, need, 0) == "LB_ERR_SHAPE"
+    assert _status(lb.lb_gemm, Wk, A16, lb.LB_BF16, 1 << 20, A16, lb.LB_BF16, A16, need, 0) == "LB_ERR_WORKSPACE"
 
 
 def test_ternary5_entry_points():
@@ -173,7 +177,8 @@ def test_gemv_batched_validation():
     assert _status(lb.lb_gemv_batched, [ok, (W1, A16, MIS)], lb.LB_F16, 1) == "LB_ERR_ALIGN"
     assert _status(lb.lb_gemv_batched, [ok, (lb.make_weight(1, 16, 130, A16, A16), A16, A16)], lb.LB_F16, 1) == "LB_ERR_SHAPE"
     # the documented k limits (an 8-CTA split), for the grouped and the single call
-    for batch, kmax in ((1, 352256), (2, 196608), (4, 98304), (8, 49152)):
-        long_w = lb.make_weight(lb.LB_FMT_1BIT_G128, 16, kmax + 128, A16, A16)
-        assert _status(lb.lb_gemv_batched, [(long_w, A16, A16)], lb.LB_F16, batch) == "LB_ERR_UNSUPPORTED"
-        assert _status(lb.lb_gemv, long_w, A16, lb.LB_F16, batch, A16, 0) == "LB_ERR_UNSUPPORTED"
+    for fmt, limits in GEMV_K_LIMITS.items():
+        for batch, kmax in limits:
+            long_w = lb.make_weight(fmt, 16, kmax + 128, A16, A16)
+            assert _status(lb.lb_gemv_batched, [(long_w, A16, A16)], lb.LB_F16, batch) == "LB_ERR_UNSUPPORTED"
+            assert _status(lb.lb_gemv, long_w, A16, lb.LB_F16, batch, A16, 0) == "LB_ERR_UNSUPPORTED"
