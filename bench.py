@@ -2,23 +2,26 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-rows]
 
-Headline workload (one JSON line on stdout, rank 0): the ternary decode layer set of a 1.7B-class
-block (q, k, v, o 2048x2048; gate, up 6144x2048; down 2048x6144; codes iid {-1,0,+1} with
-p = (0.3, 0.4, 0.3); scales |N(0, 0.02)| in fp16; x fp16 N(0, 1); batch 1).  One step decodes one
-token through LAYERS distinct copies of that layer set, each issued the way a decoder layer issues
-it: [q, k, v] on one activation vector (one lb_gemv_batched launch), [o] (lb_gemv), [gate, up] on
-one vector (lb_gemv_batched), [down] (lb_gemv), i.e. 4 launches per copy.  The weights a step
-streams (~525 MB) exceed 4x the 126 MB L2, so every step reads them from HBM.  The K timed
-steps are one CUDA-graph replay, timed with CUDA events on the launching stream.
+Headline workload (one JSON line on stdout, rank 0): the ternary decode layer set of a 27B-class
+block (hidden 5120, FFN 17408: q, o 5120x5120; gate, up 17408x5120; down 5120x17408; codes iid
+{-1,0,+1} with p = (0.3, 0.4, 0.3); scales |N(0, 0.02)| in fp16; x bf16 N(0, 1); batch 1), the
+largest decode configuration of the workload list.  One step decodes one token through LAYERS
+distinct copies of that layer set, each issued the way a decoder layer issues it: [q] (lb_gemv),
+[o] (lb_gemv), [gate, up] on one activation vector (one lb_gemv_batched launch), [down]
+(lb_gemv), i.e. 4 launches per copy.  The weights a step streams (~680 MB) exceed 4x the 126 MB
+L2, so every step reads them from HBM.  The K timed steps are one CUDA-graph replay, timed with
+CUDA events on the launching stream.
 
 ``value`` is the algorithmic packed-weight bandwidth (packed codes + scales + x + y bytes per step
 divided by the step time), in GB/s.  ``rows`` adds the other steps of the path measured the same
-way: both packers, the 1-bit GEMVs (2048x2048 fp16; 151936x2048 LM head bf16 at batch 1 and 4;
-27B-class layer sets at batch 1 and 5, both formats) and the ternary prefill GEMM (512 x 5120 ->
-17408, TFLOP/s).  ``e2e`` is the headline metric measured through the public API with host
-buffers: every step copies x from pinned host memory, runs the layer-set GEMVs and copies y back.
+way: both packers, the GEMVs of every decode configuration (1-bit 2048x2048 fp16; the 1.7B-class
+ternary layer set; the 151936x2048 LM head at batch 1 and 4; the 27B-class layer sets at batch 1
+and 5, both formats), the prefill GEMM (512 x 5120 -> 17408, TFLOP/s), the embedding gather, the
+SiLU-gated pair, and the read-only reference launches of the same byte counts (lb_read_probe).
+``e2e`` is the headline metric measured through the public API with host buffers: every step
+copies x from pinned host memory, runs the layer-set GEMVs and copies y back.
 
-``--impl reference`` times the CPU oracle (FP64 numpy) on the same workload instead.
+``--impl reference`` times the CPU oracle (FP64 numpy) on a bounded sample of the same workload.
 With torchrun (N > 1) every rank runs an independent replica (the products shard by rows without
 any exchange); value is the sum over ranks divided by the slowest rank's time.
 """
@@ -43,12 +46,12 @@ if ROOT not in sys.path:
 
 from gemm_lb_gemv_02_b300 import synth  # noqa: E402
 
-LAYERS = 36                      # distinct layer-set copies per step (weights >> L2)
-# DRAM bytes per headline GEMV launch from an ncu capture of one layer set (14.62 MB / 4 launches);
-# the algorithmic bytes are 14.55 MB per set, so nothing is re-read.  Set to None when the kernel
-# changes until a new capture is taken.
-GEMV_TRAFFIC_PER_LAUNCH = 3.662e6
+HEADLINE = "c4t"                 # the 27B-class ternary decode layer set
+LAYERS = 8                       # distinct layer-set copies per step (8 x 85 MB >> L2)
 L2_BYTES = 126 * 2 ** 20
+# ncu DRAM bytes of the headline layer set, tied to the GEMV source they were measured on
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemv_traffic.json")
+GEMV_SOURCE = os.path.join(ROOT, "gemm_lb_gemv_02_b300", "csrc", "lb_gemv.cu")
 METRIC = "packed-weight GEMV HBM GB/s (% of peak) at batch 1; prefill GEMM TFLOP/s"
 
 
@@ -270,6 +273,7 @@ def _want(name, sel):
 
 GEMV_ROWS = (  # row name, workload, batch, grouping[, storage]
     ("gemv_c1_b1", "c1", 1, "separate"),
+    ("gemv_c2_b1", "c2", 1, "layer"),
     ("gemv_c2_b1_7launches", "c2", 1, "separate"),
     ("gemv_c2_b1_1launch", "c2", 1, "one"),
     ("gemv_c3_b1", "c3", 1, "separate"),
@@ -417,6 +421,49 @@ def measure_copy_reference(peaks, sel=None):
                    "note": "library copy, not this library's kernel: the bandwidth one launch of this size reaches"}}
 
 
+def measure_read_probe_rows(lbt, peaks, sel=None):
+    """The practical read ceiling of one launch: lb_read_probe (plain 16-byte loads, the GEMV's
+    launch behaviour) over the byte counts of the headline's launches and of the LM-head GEMV,
+    rotated over > 4x L2 and graph-timed exactly like the GEMV rows.  The layer-set row issues the
+    headline's four byte counts in sequence, as the headline issues its four launches."""
+    from gemm_lb_gemv_02_b300 import lb as lbl
+    rows = {}
+    wl = synth.WORKLOADS[HEADLINE]
+    mats = {m.name: m for m in wl.matrices}
+
+    def gemv_bytes(names, batch=1):
+        by = 0
+        for nm in names:
+            m = mats[nm]
+            cb, sb = lbl.lb_packed_bytes(lbl.FORMATS[wl.fmt], m.n, m.k)
+            by += cb + sb + 2 * batch * m.n
+        return by + 2 * batch * mats[names[0]].k
+    c3 = synth.WORKLOADS["c3"].matrices[0]
+    cb3, sb3 = lbl.lb_packed_bytes(lbl.LB_FMT_1BIT_G128, c3.n, c3.k)
+    launches = [gemv_bytes(grp) for grp in LAYER_GROUPING[HEADLINE]]
+    cases = [("read_probe_c3_44MB", [cb3 + sb3 + 2 * (c3.n + c3.k)])]
+    cases += [(f"read_probe_{HEADLINE}_{'_'.join(grp)}", [b]) for grp, b in zip(LAYER_GROUPING[HEADLINE], launches)]
+    cases.append((f"read_probe_{HEADLINE}_layer_set", launches))
+    sink = torch.zeros(4, dtype=torch.int32, device="cuda")
+    for name, sizes in cases:
+        if not _want(name, sel):
+            continue
+        sizes = [(b + 15) // 16 * 16 for b in sizes]
+        copies = _copies_for(sum(sizes))
+        bufs = [[torch.empty(b, dtype=torch.uint8, device="cuda") for b in sizes] for _ in range(copies)]
+        steps = copies * 2
+        g = _graph(lambda: [lbl.lb_read_probe(buf, buf.numel(), sink) for i in range(steps) for buf in bufs[i % copies]])
+        _time_graph(g)
+        ms = _time_graph(g, reps=3) / steps
+        gbs = sum(sizes) / (ms * 1e-3) / 1e9
+        rows[name] = {"bytes_per_launch": sizes, "us_per_step": round(ms * 1e3, 3), "GB_s": round(gbs, 1),
+                      "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 3), "copies_rotated": copies,
+                      "note": "read-only reference launch (no compute), not the method's work"}
+        del bufs, g
+        torch.cuda.empty_cache()
+    return rows
+
+
 SWIGLU_ROWS = (  # row name, workload, batch
     ("swiglu_c2_b1", "c2", 1),
     ("swiglu_c4t_b1", "c4t", 1),
@@ -488,82 +535,147 @@ def measure_embed_rows(lbt, peaks, sel=None):
                    "bytes_basis": "codes + scales of each gathered row + ids + rows written"}}
 
 
-def cpu_baseline(seconds: float = 10.0):
-    """The oracle as it stands (FP64 numpy) on the headline layer set, repeated for ~seconds."""
+# ------------------------------------------------------------------------------------ CPU oracle
+# The oracle is timed on a bounded sample of the headline workload: the first 1/ORACLE_ROW_FRACTION of
+# the rows of every matrix of one layer set (the same K, codes, scales and x as the GPU's), so that
+# one pass is a fraction of a second.  The same sample serves the CPU-baseline leg and the
+# reference arm.
+ORACLE_ROW_FRACTION = 16
+
+
+def _oracle_sample():
     from oracle import lb_oracle as orc
-    wl = synth.WORKLOADS["c2"]
+    wl = synth.WORKLOADS[HEADLINE]
     mats = []
     for i, m in enumerate(wl.matrices):
         inp = synth.matrix_inputs(wl, i)
-        c, s = orc.pack_ternary(inp["t"].numpy(), inp["s"].numpy().view(np.uint16))
-        x = orc.f16_bits_to_f64(synth.workload_activations(wl, i, 1).view(torch.int16).numpy().view(np.uint16))
-        mats.append((c, s, m.k, x, c.nbytes + s.nbytes + 2 * (m.k + m.n)))
+        rows = m.n // ORACLE_ROW_FRACTION
+        c, s = orc.pack_ternary(inp["t"][:rows].numpy(), inp["s"][:rows].numpy().view(np.uint16))
+        x = orc.decode_activation_bits(synth.workload_activations(wl, i, 1).view(torch.int16).numpy().view(np.uint16),
+                                       wl.xdtype)
+        mats.append((c, s, m.k, x, c.nbytes + s.nbytes + 2 * (m.k + rows)))
+    return mats
+
+
+def _oracle_pass(mats) -> int:
+    from oracle import lb_oracle as orc
+    for c, s, k, x, _ in mats:
+        orc.matvec(orc.FMT_TERNARY, c, s, k, x)
+    return sum(m[4] for m in mats)
+
+
+_ORACLE_MATS = None
+
+
+def _oracle_init():
+    """Per process: one BLAS thread, and the sample built once."""
+    global _ORACLE_MATS
+    try:
+        from threadpoolctl import threadpool_limits
+        threadpool_limits(1)
+    except Exception:
+        pass
+    _ORACLE_MATS = _oracle_sample()
+    _oracle_pass(_ORACLE_MATS)                               # warm (first allocations)
+
+
+def _oracle_step(_=None) -> int:
+    return _oracle_pass(_ORACLE_MATS)
+
+
+def _oracle_timed(seconds: float):
+    """Oracle passes over this process's sample for about `seconds`."""
     done, nbytes = 0, 0
     t0 = time.perf_counter()
     while time.perf_counter() - t0 < seconds or done == 0:
-        for c, s, k, x, by in mats:
-            orc.matvec(orc.FMT_TERNARY, c, s, k, x)
-            nbytes += by
+        nbytes += _oracle_pass(_ORACLE_MATS)
         done += 1
-    dt = time.perf_counter() - t0
-    return nbytes / dt / 1e9, dt, done
+    return nbytes, time.perf_counter() - t0, done
 
 
-def _blas_threads():
+def host_cores() -> int:
     try:
-        from threadpoolctl import threadpool_info
-        return max([d.get("num_threads", 1) for d in threadpool_info()] or [1])
-    except Exception:
-        return 1
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_model() -> str:
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def cpu_baseline(seconds: float = 10.0):
+    """The oracle as it stands, timed on the host cores: in one spawned process with one thread, then
+    in one spawned process per core (so no process forks after the GPU was touched), each over the
+    whole sample; GB/s of algorithmic bytes."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(1, initializer=_oracle_init) as pool:
+        nb1, dt1, _ = pool.apply(_oracle_timed, (seconds / 2,))
+    cores = host_cores()
+    with ctx.Pool(cores, initializer=_oracle_init) as pool:
+        res = pool.map(_oracle_timed, [seconds / 2] * cores)
+    wall = max(r[1] for r in res)
+    return {"single_thread_GB_s": nb1 / dt1 / 1e9, "all_cores_GB_s": sum(r[0] for r in res) / wall / 1e9,
+            "cores": cores, "passes_all_cores": sum(r[2] for r in res), "seconds": seconds}
 
 
 # ------------------------------------------------------------------------------------ arms
 def run_reference(args, ws, rank):
     if rank != 0:
         return
-    from oracle import lb_oracle as orc
-    wl = synth.WORKLOADS["c2"]
-    frac = 8                                      # each step: 1/8 of every matrix's rows
-    mats = []
-    for i, m in enumerate(wl.matrices):
-        inp = synth.matrix_inputs(wl, i)
-        c, s = orc.pack_ternary(inp["t"].numpy(), inp["s"].numpy().view(np.uint16))
-        rows = m.n // frac
-        x = orc.f16_bits_to_f64(synth.workload_activations(wl, i, 1).view(torch.int16).numpy().view(np.uint16))
-        mats.append((c[:rows], s[:rows], m.k, x, c[:rows].nbytes + s[:rows].nbytes + 2 * (m.k + rows)))
-
-    def step():
-        for c, s, k, x, _ in mats:
-            orc.matvec(orc.FMT_TERNARY, c, s, k, x)
-
-    for _ in range(args.warmup):
-        step()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step()
-    dt = time.perf_counter() - t0
-    by = sum(m[4] for m in mats)
-    v = by * args.steps / dt / 1e9
-    sample = f"1/{frac} of the rows of each of the 7 layer-set matrices per step (FP64 numpy oracle)"
+    import multiprocessing as mp
+    cores = host_cores()
+    # each step: one pass over the sample in every one of `cores` spawned processes
+    with mp.get_context("spawn").Pool(cores, initializer=_oracle_init) as pool:
+        for _ in range(args.warmup):
+            pool.map(_oracle_step, range(cores), chunksize=1)
+        t0 = time.perf_counter()
+        nbytes = 0
+        for _ in range(args.steps):
+            nbytes += sum(pool.map(_oracle_step, range(cores), chunksize=1))
+        dt = time.perf_counter() - t0
+    v = nbytes / dt / 1e9
+    sample = (f"1/{ORACLE_ROW_FRACTION} of the rows of each of the 5 matrices of the {HEADLINE} layer set per "
+              f"process, {cores} spawned processes (one BLAS thread each), FP64 numpy oracle")
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": "GB/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": _config(),
-            "cpu_baseline": {"value": round(v, 3), "unit": "GB/s", "cores": _blas_threads(), "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": round(v, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": sample, "cpu": cpu_model()},
             "e2e": {"value": round(v, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 def _config():
-    return {"workload": "c2: ternary g128 decode layer set of a 1.7B-class block (q,k,v,o 2048x2048; "
-                        "gate,up 6144x2048; down 2048x6144), batch 1, x fp16, FP32 accumulate; "
-                        f"one step = one token through {LAYERS} distinct copies of the set, each issued as "
-                        "a decoder layer issues it: [q,k,v] on one x (one grouped launch), [o], [gate,up] on "
-                        "one x (one grouped launch), [down]",
+    return {"workload": f"{HEADLINE}: ternary g128 decode layer set of a 27B-class block (hidden 5120, FFN "
+                        "17408: q, o 5120x5120; gate, up 17408x5120; down 5120x17408), batch 1, x bf16, FP32 "
+                        f"accumulate; one step = one token through {LAYERS} distinct copies of the set, each "
+                        "issued as a decoder layer issues it: [q], [o], [gate, up] on one x (one grouped "
+                        "launch), [down]",
             "global_batch": 1, "layers_per_step": LAYERS, "parallelism": "replicas",
             "l2": f"inputs larger than L2: {LAYERS} rotated copies (> 4x 126 MB) per step",
-            "seeds": "synth.WORKLOADS['c2'].seed = 1002"}
+            "seeds": f"synth.WORKLOADS['{HEADLINE}'].seed = {synth.WORKLOADS[HEADLINE].seed}"}
+
+
+def _traffic_per_launch():
+    """ncu DRAM bytes per headline launch, if they were measured on the current GEMV source."""
+    import hashlib
+    try:
+        rec = json.load(open(TRAFFIC_FILE))
+        sha = hashlib.sha256(open(GEMV_SOURCE, "rb").read()).hexdigest()
+    except (OSError, ValueError):
+        return None, "no capture on record"
+    if rec.get("gemv_source_sha256") != sha:
+        return None, "the GEMV source changed since the last capture"
+    return rec.get("dram_bytes_per_launch"), rec.get("basis", "")
 
 
 def run_ours(args, ws, rank, local):
@@ -571,11 +683,12 @@ def run_ours(args, ws, rank, local):
     from gemm_lb_gemv_02_b300 import tensors as lbt
     torch.cuda.set_device(local)
     peaks = _peaks()
-    wl = synth.WORKLOADS["c2"]
+    wl = synth.WORKLOADS[HEADLINE]
     gs = GemvSet(wl, 1, lbt, copies=LAYERS, layers_per_step=LAYERS, grouping="layer")
     warm = _graph(lambda: [gs.step() for _ in range(max(1, args.warmup))])
     timed = _graph(lambda: [gs.step() for _ in range(args.steps)])
-    launches = args.steps * LAYERS * gs.launches_per_layer
+    launches_per_layer = gs.launches_per_layer
+    launches = args.steps * LAYERS * launches_per_layer
 
     with ClockSampler(local) as clocks:
         # soak: keep the same load running for ~1.5 s so that the sampler sees it (one replay in
@@ -602,7 +715,7 @@ def run_ours(args, ws, rank, local):
 
     # end to end through the public API with host buffers: per step the token's activation
     # vectors (one per launch group) come from pinned host memory, all layers run eagerly through
-    # lb_gemv / lb_gemv_batched, and the 7 outputs of the last layer are read back
+    # lb_gemv / lb_gemv_batched, and the outputs of the last layer are read back
     heads = sorted({id(gs.x[i]): i for grp in gs.groups for i in grp}.values())   # distinct vectors
     xs_h = {i: gs.x[i].cpu().pin_memory() for i in heads}
     ys_h = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in gs.y]
@@ -663,33 +776,38 @@ def run_ours(args, ws, rank, local):
         rows.update(measure_gemm_row(lbt, peaks, sel))
         rows.update(measure_embed_rows(lbt, peaks, sel))
         rows.update(measure_swiglu_rows(lbt, peaks, sel))
+        rows.update(measure_read_probe_rows(lbt, peaks, sel))
         rows.update(measure_copy_reference(peaks, sel))
     assert lbl.lb_device_error(clear=True) == 0, "device error word set"
 
     if rank != 0:
         return
-    cpu_v, cpu_dt, cpu_passes = cpu_baseline(args.cpu_seconds)
+    cpu = cpu_baseline(args.cpu_seconds)
+    traffic, traffic_basis = _traffic_per_launch()
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic", "config": _config(),
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": _config(),
         "roofline": {"bound": "hbm", "achieved": round(per_rank_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(per_rank_gbs / peaks["hbm_gbs"], 4), "traffic": GEMV_TRAFFIC_PER_LAUNCH,
-                     "traffic_basis": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one layer set "
-                                      "(4 launches) / 4, bytes per launch; kernel as of commit 2b2edaa "
-                                      "(summary under profiles/, gemv_kernel on the c2 layer set)",
-                     "kernel": "gemv_kernel<ternary, f16 x, batch 1> (4 launches per layer set: "
-                               "q/k/v grouped, o, gate/up grouped, down)",
+                     "frac": round(per_rank_gbs / peaks["hbm_gbs"], 4), "traffic": traffic,
+                     "traffic_basis": traffic_basis,
+                     "kernel": "gemv_kernel<ternary, bf16 x, batch 1> (4 launches per layer set: q, o, "
+                               "gate/up grouped, down)",
                      "achieved_basis": "algorithmic bytes (packed codes + scales + x + y) per launch / "
                                        "(timed region / launches), CUDA events, so launch gaps count against it",
+                     "algorithmic_bytes_per_launch": round(by_step / (LAYERS * launches_per_layer)),
                      "peak_basis": f"{peaks['source']} STREAM-style copy bandwidth"},
-        "cpu_baseline": {"value": round(cpu_v, 3), "unit": "GB/s", "cores": _blas_threads(), "kind": "oracle",
-                         "sample": f"the full layer set (7 matrices, 54.5 M weights), {cpu_passes} passes in "
-                                   f"{cpu_dt:.1f} s, FP64 numpy oracle"},
+        "cpu_baseline": {"value": round(cpu["all_cores_GB_s"], 4), "unit": "GB/s", "cores": cpu["cores"],
+                         "kind": "oracle", "cpu": cpu_model(),
+                         "single_thread_value": round(cpu["single_thread_GB_s"], 4),
+                         "sample": f"1/{ORACLE_ROW_FRACTION} of the rows of each matrix of the {HEADLINE} layer set, "
+                                   f"FP64 numpy oracle; one spawned process per core with one BLAS thread each, "
+                                   f"{cpu['passes_all_cores']} passes in {cpu['seconds'] / 2:.1f} s (value), and "
+                                   "one process with one thread (single_thread_value)"},
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "how": "per step: the 4 activation vectors (one per launch group) copied from pinned host "
+                "how": "per step: the activation vectors (one per launch group) copied from pinned host "
                        "memory, LAYERS x 4 eager lb_gemv / lb_gemv_batched calls through the Python binding, "
-                       "the 7 outputs copied back, one stream synchronize; host wall clock, after 0.3 s of "
+                       "the outputs copied back, one stream synchronize; host wall clock, after 0.3 s of "
                        "the same load and W warm-up steps (an idle GPU's lowered clocks are not raised "
                        "again by this host-paced loop)",
                 "graph_value": round(e2e_graph_value, 1),
@@ -701,6 +819,19 @@ def run_ours(args, ws, rank, local):
         "rows": rows,
     }
     print(json.dumps(line), flush=True)
+
+
+def run_rows_only(args, local):
+    from gemm_lb_gemv_02_b300 import tensors as lbt
+    torch.cuda.set_device(local)
+    peaks = _peaks()
+    sel = [r for r in args.rows.split(",") if r] if args.rows not in ("all", "none") else None
+    rows = {}
+    rows.update(measure_gemv_rows(lbt, peaks, sel))
+    rows.update(measure_gemm_row(lbt, peaks, sel))
+    rows.update(measure_swiglu_rows(lbt, peaks, sel))
+    rows.update(measure_read_probe_rows(lbt, peaks, sel))
+    print(json.dumps({"rows_only": True, "rows": rows}), flush=True)
 
 
 def main():
@@ -716,6 +847,9 @@ def main():
     ap.add_argument("--soak", type=float, default=1.5,
                     help="seconds of untimed load before the timed region (clock sampling)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline duration")
+    ap.add_argument("--rows-only", action="store_true",
+                    help="measure only the rows selected by --rows and print them (no headline, e2e or CPU "
+                         "leg); for profiling one kernel under ncu")
     args = ap.parse_args()
     ws, rank, local = _dist()
     if ws > 1:
@@ -726,6 +860,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, ws, rank)
+        elif args.rows_only:
+            run_rows_only(args, local)
         else:
             run_ours(args, ws, rank, local)
     finally:
