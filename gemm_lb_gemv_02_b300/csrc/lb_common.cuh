@@ -136,6 +136,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   } while (globaltimer_ns() - t0 < limit_ns);
   return false;
 }
+// Bounded wait for a thread that is usually far ahead of the phase it waits for (a producer
+// waiting for a free ring slot): between polls it sleeps on the SM's nanosleep timer, so that its
+// warp issues almost nothing while it waits and leaves the issue slots of its sub-partition to the
+// warps that do the work.
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  do {
+    __nanosleep(128);
+    if (mbar_try_wait(bar, parity)) return true;
+  } while (globaltimer_ns() - t0 < limit_ns);
+  return false;
+}
 
 // async proxy / bulk copies -------------------------------------------------------------------
 __device__ __forceinline__ void fence_proxy_async_smem() {

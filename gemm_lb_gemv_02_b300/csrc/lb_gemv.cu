@@ -241,9 +241,11 @@ struct Layout {
   static constexpr int colf = red + 2 * ROWS * 8 * 4;            // 8 column factors + 8 column maxima
   static constexpr int cneg = colf + 64;                         // gpc x 4 x float4 {-C[2q], -C[2q+1], same}
   static constexpr int xgroup = 4 * 4 * BP * 16;                 // x fragments of one group
-  __host__ __device__ static int xs(int gpc) { return cneg + gpc * 64; }
+  // the x fragments and baselines are padded to whole stages (zeros), so a stage is always full
+  __host__ __device__ static int pad(int gpc) { return (gpc + GS - 1) / GS * GS; }
+  __host__ __device__ static int xs(int gpc) { return cneg + pad(gpc) * 64; }
   // + 512 bytes that lanes outside the batch may read past the last group, + 1024 alignment slack
-  __host__ __device__ static int total(int gpc) { return xs(gpc) + gpc * xgroup + 512 + 1024; }
+  __host__ __device__ static int total(int gpc) { return xs(gpc) + pad(gpc) * xgroup + 512 + 1024; }
 };
 
 template <int FMT, bool XBF, int BP>
@@ -314,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
       const uint32_t bytes = static_cast<uint32_t>(FT::nb * kBox + (P.scales_tma ? kScaleBox : 0));
       for (int st = 0; st < total_st && !a.test_fault; ++st) {
         const int s = st % L::stages;
-        if (!lbdev::mbar_wait(&empty[s], static_cast<uint32_t>(((st / L::stages) & 1) ^ 1), a.wait_ns)) {
+        if (!lbdev::mbar_wait_backoff(&empty[s], static_cast<uint32_t>(((st / L::stages) & 1) ^ 1), a.wait_ns)) {
           ok = false;
           break;
         }
@@ -454,9 +456,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
       }
     }
     if (FMT == 1) {
-      for (int i = threadIdx.x; i < ng * 16; i += NW * 32)          // columns beyond the padded batch
-        if (((i >> 2) & 3) * 2 + (i & 1) >= BP) cneg[i] = 0.f;
+      // columns beyond the padded batch, and every column of the groups that pad the last stage
+      for (int i = threadIdx.x; i < L::pad(ng) * 16; i += NW * 32)
+        if (i >= ng * 16 || ((i >> 2) & 3) * 2 + (i & 1) >= BP) cneg[i] = 0.f;
     }
+    for (int i = ng * (L::xgroup / 16) + threadIdx.x; i < L::pad(ng) * (L::xgroup / 16); i += NW * 32)
+      reinterpret_cast<uint4*>(xs)[i] = make_uint4(0u, 0u, 0u, 0u);  // x of the padding groups: zero
     consumer_sync();
 
     uint32_t tok;                                      // orders the private-region loads after the barrier
@@ -543,36 +548,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
       if (lane == 0) lbdev::mbar_arrive(&empty[s]);               // slot s released by this warp
       if (++s == L::stages) { s = 0; ph ^= 1u; }
 
-      if (ok && cnt > 0) {
+      if (ok && cnt > 0) {                                        // cnt <= 0: a half with no groups
         const uint32_t xbase = xs_lane + static_cast<uint32_t>(g0 * L::xgroup);
         const uint32_t cbase = cn_q + static_cast<uint32_t>(g0 * 64);
-        // one group j (single accumulator chain); used for a ragged last stage
-        auto one_group = [&](int j) {
-          Word1 w1a = prep1(ca[j].x), w1b = prep1(cb[j].x);
-          Word2 wla = prep2(ca[j].x), wha = prep2(ca[j].y), wlb = prep2(cb[j].x), whb = prep2(cb[j].y);
-          const float4 cn = FMT == 1 ? lds128f(cbase + j * 64) : make_float4(0.f, 0.f, 0.f, 0.f);
-          uint4 bx[4];
-#pragma unroll
-          for (int iq = 0; iq < 4; ++iq) bx[iq] = lds128(xbase + j * L::xgroup + iq * (L::xgroup / 4));
-          float d[4];
-#define LB_ONE(I)                                                                                          \
-  {                                                                                                        \
-    const uint32_t blo = (I) % 2 == 0 ? bx[(I) / 2].x : bx[(I) / 2].z;                                      \
-    const uint32_t bhi = (I) % 2 == 0 ? bx[(I) / 2].y : bx[(I) / 2].w;                                      \
-    const uint32_t e0 = areg<FMT, 2 * (I)>(w1a, wla, wha, M, SC), e1 = areg<FMT, 2 * (I)>(w1b, wlb, whb, M, SC);      \
-    const uint32_t e2 = areg<FMT, 2 * (I) + 1>(w1a, wla, wha, M, SC), e3 = areg<FMT, 2 * (I) + 1>(w1b, wlb, whb, M, SC); \
-    if ((I) == 0) mma_c4(d, e0, e1, e2, e3, blo, bhi, cn);                                                 \
-    else mma_acc(d, e0, e1, e2, e3, blo, bhi);                                                             \
-  }
-          LB_ONE(0) LB_ONE(1) LB_ONE(2) LB_ONE(3) LB_ONE(4) LB_ONE(5) LB_ONE(6) LB_ONE(7)
-#undef LB_ONE
-          acc[0] = fmaf(sa[j], d[0], acc[0]);
-          acc[1] = fmaf(sa[j], d[1], acc[1]);
-          acc[2] = fmaf(sb[j], d[2], acc[2]);
-          acc[3] = fmaf(sb[j], d[3], acc[3]);
-        };
-        if (cnt == GH) {
-          // full stage: two pairs of groups, two independent accumulator chains per pair
+        {
+          // a stage is always full (codes and scales past the end of K arrive as zeros, and the x
+          // of the padding groups is zero): two pairs of groups, two accumulator chains per pair
 #pragma unroll
           for (int jp = 0; jp < GH; jp += 2) {
             Word1 w1a0 = prep1(ca[jp].x), w1b0 = prep1(cb[jp].x), w1a1 = prep1(ca[jp + 1].x), w1b1 = prep1(cb[jp + 1].x);
@@ -618,10 +599,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             acc[2] = fmaf(sb[jp + 1], d1[2], acc[2]);
             acc[3] = fmaf(sb[jp + 1], d1[3], acc[3]);
           }
-        } else {
-#pragma unroll
-          for (int j = 0; j < GH; ++j)
-            if (j < cnt) one_group(j);
         }
       }
 
