@@ -40,16 +40,21 @@ def _stale(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, trace: bool = False) -> str:
+    """trace=True: the phase-trace variant (-DLB_GEMV_TRACE) as liblb_trace.so, objects in
+    _build_trace/; the product library is untouched."""
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    build_dir = BUILD + "_trace" if trace else BUILD
+    lib = os.path.join(HERE, "liblb_trace.so") if trace else LIB
+    extra = ["-DLB_GEMV_TRACE"] if trace else []
+    os.makedirs(build_dir, exist_ok=True)
     headers = glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(ROOT, "include", "*.h"))
     objs, jobs = [], []
     for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + headers):
-            cmd = [nvcc, *ARCH, *FLAGS, "-c", src, "-o", obj]
+            cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
             if verbose:
                 cmd += ["-Xptxas", "-v"]
             jobs.append(cmd)
@@ -64,18 +69,19 @@ def build(force: bool = False, verbose: bool = False) -> str:
                 sys.stderr.write(r.stdout + r.stderr)
             if r.returncode:
                 raise RuntimeError(f"nvcc failed: {' '.join(cmd)}")
-    if force or jobs or _stale(LIB, objs):
-        cmd = [nvcc, *ARCH, "-shared", "-o", LIB, *objs]
+    if force or jobs or _stale(lib, objs):
+        cmd = [nvcc, *ARCH, "-shared", "-o", lib, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode:
             sys.stderr.write(r.stdout + r.stderr)
             raise RuntimeError("nvcc link failed")
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose", action="store_true")
+    ap.add_argument("--trace", action="store_true", help="build the phase-trace variant liblb_trace.so")
     a = ap.parse_args()
-    print(build(force=a.force, verbose=a.verbose))
+    print(build(force=a.force, verbose=a.verbose, trace=a.trace))

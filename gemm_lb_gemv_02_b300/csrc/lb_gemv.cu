@@ -69,12 +69,10 @@ struct FmtTraits;
 template <>
 struct FmtTraits<1> {                     // 1-bit: 16 B per group per row, 8 groups per box
   static constexpr int gbytes = 16, nb = 1, stages = 6;
-  static constexpr float h = 0.5f;
 };
 template <>
 struct FmtTraits<2> {                     // ternary: 32 B per group per row, 4 groups per box
   static constexpr int gbytes = 32, nb = 2, stages = 3;
-  static constexpr float h = 1.0f;
 };
 
 // ----------------------------------------------------------------------------- decode
@@ -146,6 +144,13 @@ __device__ __forceinline__ void mma_c4(float (&d)[4], uint32_t a0, uint32_t a1, 
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c.x), "f"(c.y), "f"(c.z), "f"(c.w));
 }
+// D = A * B (the accumulator starts from zero).
+__device__ __forceinline__ void mma_zero(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
 __device__ __forceinline__ void mma_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
   asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
@@ -175,7 +180,34 @@ __device__ __forceinline__ float ld_dsmem(uint32_t local_addr, uint32_t rank) {
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
   return v;
 }
+// Phase trace (compiled in only with -DLB_GEMV_TRACE, for timing studies): per CTA, event e holds
+// {%globaltimer, clock64} of the moment one fixed thread passed a point of the kernel.  Events:
+// 0 CTA start, 1 producer's first copy issued, 2 producer's last copy issued, 3 consumers past
+// griddepcontrol.wait, 4 x prologue done, 5 + i (i < 16) warp 0 got stage i, 21 + j (j < 8) warp
+// 0 finished unit j, 29 consumers done, 30 CTA end; slot 31 holds {gridDim.x, gridDim.y}.
+#ifdef LB_GEMV_TRACE
+constexpr int kTraceCtas = 2048, kTraceEvents = 32;
+__device__ unsigned long long g_gemv_trace[kTraceCtas][kTraceEvents][2];
+__device__ __forceinline__ void trace_ev(int e) {
+  const unsigned cta = blockIdx.y * gridDim.x + blockIdx.x;
+  if (cta < kTraceCtas && e < kTraceEvents) {
+    g_gemv_trace[cta][e][0] = lbdev::globaltimer_ns();
+    g_gemv_trace[cta][e][1] = static_cast<unsigned long long>(clock64());
+  }
+}
+#define LB_TRACE(cond, e) \
+  do {                    \
+    if (cond) trace_ev(e); \
+  } while (0)
+#else
+#define LB_TRACE(cond, e) \
+  do {                    \
+  } while (0)
+#endif
+
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(NW * 32) : "memory"); }
+// the two consumer warps of 16-row tile t (named barriers 2 .. NT + 1)
+__device__ __forceinline__ void tile_sync(int t) { asm volatile("bar.sync %0, 64;" ::"r"(2 + t) : "memory"); }
 
 // Shared-memory loads with 32-bit shared addresses.  Loads from a pipeline slot are volatile, so
 // they stay between the barrier wait that makes the slot valid and the arrive that hands it back.
@@ -258,6 +290,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   uint64_t* empty = full + L::stages;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  LB_TRACE(threadIdx.x == 0, 0);
+#ifdef LB_GEMV_TRACE
+  if (threadIdx.x == 0 && blockIdx.y * gridDim.x + blockIdx.x < kTraceCtas) {   // which launch wrote the CTA's events
+    g_gemv_trace[blockIdx.y * gridDim.x + blockIdx.x][kTraceEvents - 1][0] = gridDim.x;
+    g_gemv_trace[blockIdx.y * gridDim.x + blockIdx.x][kTraceEvents - 1][1] = gridDim.y;
+  }
+#endif
   int pi = 0;                                                    // this CTA's problem
   for (int i = 1; i < a.count && !a.fuse; ++i)
     if (static_cast<int>(blockIdx.y) >= a.p[i].unit0) pi = i;
@@ -297,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < L::stages; ++s) {
-      lbdev::mbar_init(&full[s], 1);
+      lbdev::mbar_init(&full[s], P.scales_tma ? 1 : 32);         // 32: the lanes store the scales
       lbdev::mbar_init(&empty[s], NW);
     }
     lbdev::fence_mbar_init();
@@ -306,14 +345,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   __syncthreads();
 
   if (warp == NW) {
-    // ======================= producer: weights do not depend on earlier kernels, so no wait
-    if (lane == 0) {
+    // ======================= producer: weights do not depend on earlier kernels, so no wait.
+    // Codes (and scales, when a scale row is a multiple of 16 bytes) arrive by TMA; otherwise the
+    // 32 lanes load the stage's scales from global memory, store them in the slot in the TMA
+    // box's layout and arrive on the stage's barrier themselves.
+    const bool stma = P.scales_tma != 0;
+    if (lane == 0)
       for (int i = 0; i < a.count; ++i)
         if (i == pi || a.fuse || a.shared) {
           lbdev::prefetch_tmap(&a.p[i].tm_codes);
-          if (P.scales_tma) lbdev::prefetch_tmap(&a.p[i].tm_scales);
+          if (stma) lbdev::prefetch_tmap(&a.p[i].tm_scales);
         }
-      const uint32_t bytes = static_cast<uint32_t>(FT::nb * kBox + (P.scales_tma ? kScaleBox : 0));
+    const uint32_t bytes = static_cast<uint32_t>(FT::nb * kBox + (stma ? kScaleBox : 0));
+    if (stma ? lane == 0 : true) {
       for (int st = 0; st < total_st && !a.test_fault; ++st) {
         const int s = st % L::stages;
         if (!lbdev::mbar_wait_backoff(&empty[s], static_cast<uint32_t>(((st / L::stages) & 1) ^ 1), a.wait_ns)) {
@@ -324,11 +368,33 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         const Prob& PU = a.p[unit_prob(st / nst)];                 // the matrix of this unit
         const int g0 = g_begin + (st % nst) * GS;
         uint8_t* slot = sm + s * L::slot;
-        lbdev::mbar_arrive_expect_tx(&full[s], bytes);
+        if (!stma) {
+          // rows row0 + lane + 32i, groups g0 .. g0 + 7; zero outside the matrix, as TMA fills
 #pragma unroll
-        for (int b = 0; b < FT::nb; ++b)
-          lbdev::tma_load_2d(slot + b * kBox, &PU.tm_codes, (g0 + b * (GS / FT::nb)) * FT::gbytes, row0, &full[s]);
-        if (P.scales_tma) lbdev::tma_load_2d(slot + FT::nb * kBox, &PU.tm_scales, g0, row0, &full[s]);
+          for (int i = 0; i < 4; ++i) {
+            const int row = row0 + lane + 32 * i;
+            uint32_t v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int g = g0 + 2 * j;
+              const uint16_t* src = PU.scales + static_cast<int64_t>(row) * PU.G + g;
+              const uint32_t lo = (row < PU.n && g < PU.G) ? __ldg(src) : 0u;
+              const uint32_t hi = (row < PU.n && g + 1 < PU.G) ? __ldg(src + 1) : 0u;
+              v[j] = lo | (hi << 16);
+            }
+            *reinterpret_cast<uint4*>(slot + FT::nb * kBox + (lane + 32 * i) * 16) = make_uint4(v[0], v[1], v[2], v[3]);
+          }
+          if (lane != 0) lbdev::mbar_arrive(&full[s]);
+        }
+        if (lane == 0) {
+          lbdev::mbar_arrive_expect_tx(&full[s], bytes);
+#pragma unroll
+          for (int b = 0; b < FT::nb; ++b)
+            lbdev::tma_load_2d(slot + b * kBox, &PU.tm_codes, (g0 + b * (GS / FT::nb)) * FT::gbytes, row0, &full[s]);
+          if (stma) lbdev::tma_load_2d(slot + FT::nb * kBox, &PU.tm_scales, g0, row0, &full[s]);
+          LB_TRACE(st == 0, 1);
+          LB_TRACE(st == total_st - 1, 2);
+        }
       }
     }
     __syncwarp();
@@ -341,6 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     float* cneg = reinterpret_cast<float*>(sm + L::cneg);            // [gpc][4][4]
     uint8_t* xs = sm + L::xs(gpc);
     griddep_wait();                                   // x is read and y written only after this
+    LB_TRACE(threadIdx.x == 0, 3);
 
     // ---- x prologue.  Tuple (g, n, qq): the 32 activations x[n][128(g_begin+g) + 32qq ..] of one
     // fragment lane.  bfloat16 columns are scaled by an exact power of two 2^p that puts the
@@ -463,6 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     for (int i = ng * (L::xgroup / 16) + threadIdx.x; i < L::pad(ng) * (L::xgroup / 16); i += NW * 32)
       reinterpret_cast<uint4*>(xs)[i] = make_uint4(0u, 0u, 0u, 0u);  // x of the padding groups: zero
     consumer_sync();
+    LB_TRACE(threadIdx.x == 0, 4);
 
     uint32_t tok;                                      // orders the private-region loads after the barrier
     asm volatile("mov.u32 %0, 0;" : "=r"(tok)::"memory");
@@ -486,55 +554,42 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
       pcode = static_cast<uint32_t>(ia * 128) | (8u * (q & 1)) | (static_cast<uint32_t>((q >> 1) ^ r) << 4);
       pcode += static_cast<uint32_t>(half * kBox);                 // ternary: one box per half
     }
+    uint32_t pc[GH];                                               // my words of group j of a stage
+#pragma unroll
+    for (int j = 0; j < GH; ++j) pc[j] = pcode ^ (static_cast<uint32_t>(j) << (FMT == 1 ? 4 : 5));
     const uint32_t sm32 = lbdev::smem_u32(sm);
     const uint32_t xs_lane = sm32 + static_cast<uint32_t>(L::xs(gpc)) + lane * 16 + tok;
     const uint32_t cn_q = sm32 + static_cast<uint32_t>(L::cneg) + 16 * q + tok;
     const uint32_t sc_off = static_cast<uint32_t>(FT::nb * kBox + ia * 16 + half * 8);
     const float mul = FMT == 1 ? 2.f : 1.f;
     const int c0col = 2 * q, c1col = 2 * q + 1;
-    const float f0 = colf[c0col] * mul, f1 = colf[c1col] * mul;   // output factors of my columns
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    float gate[4] = {0.f, 0.f, 0.f, 0.f};                         // fused pair, S == 1: the gate outputs
     int s = 0, cstage = 0, i_rb = 0;
     uint32_t ph = 0;
 
     for (int st = 0; st < total_st; ++st) {
-      const int rb = unit_rb(i_rb);
-      const Prob& PU = a.p[unit_prob(i_rb)];                      // the matrix of this unit
       const int g0 = cstage * GS + half * GH;                     // my first group, relative to g_begin
       const int cnt = min(GH, ng - g0);                           // my groups in this stage (may be <= 0)
       const uint32_t slot = sm32 + static_cast<uint32_t>(s * L::slot);
       float sa[GH], sb[GH];
-      if (!P.scales_tma) {                                        // fallback: scales from L2
-        const int row_a = rb * ROWS + ia, row_b = row_a + 8;
-#pragma unroll
-        for (int j = 0; j < GH; ++j) {
-          sa[j] = 0.f; sb[j] = 0.f;
-          if (j < cnt) {
-            const int64_t g = g_begin + g0 + j;
-            if (row_a < PU.n) sa[j] = __half2float(__ushort_as_half(__ldg(PU.scales + static_cast<int64_t>(row_a) * PU.G + g)));
-            if (row_b < PU.n) sb[j] = __half2float(__ushort_as_half(__ldg(PU.scales + static_cast<int64_t>(row_b) * PU.G + g)));
-          }
-        }
-      }
       if (ok && !lbdev::mbar_wait(&full[s], ph, a.wait_ns)) ok = false;
       ok = __all_sync(0xffffffffu, ok);
+      LB_TRACE(threadIdx.x == 0 && st < 16, 5 + st);
       // ---- the stage's codes and scales -> registers, then the slot goes back to the producer
       uint2 ca[GH], cb[GH];                                        // rows ia / ia + 8, my 4 groups
       if (ok) {
 #pragma unroll
         for (int j = 0; j < GH; ++j) {
+          const uint32_t o = slot + pc[j];
           if (FMT == 1) {
-            const uint32_t o = slot + (pcode ^ (static_cast<uint32_t>(j) << 4));
             ca[j] = make_uint2(ldsv32(o), 0u);
             cb[j] = make_uint2(ldsv32(o + 1024), 0u);
           } else {
-            const uint32_t o = slot + (pcode ^ (static_cast<uint32_t>(j) << 5));
             ca[j] = ldsv64(o);
             cb[j] = ldsv64(o + 1024);
           }
         }
-        if (P.scales_tma) {
+        {
           const uint2 va = ldsv64(slot + sc_off), vb = ldsv64(slot + sc_off + 128);
           const float2 a01 = __half22float2(*reinterpret_cast<const __half2*>(&va.x));
           const float2 a23 = __half22float2(*reinterpret_cast<const __half2*>(&va.y));
@@ -559,8 +614,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             Word1 w1a0 = prep1(ca[jp].x), w1b0 = prep1(cb[jp].x), w1a1 = prep1(ca[jp + 1].x), w1b1 = prep1(cb[jp + 1].x);
             Word2 la0 = prep2(ca[jp].x), ha0 = prep2(ca[jp].y), lb0 = prep2(cb[jp].x), hb0 = prep2(cb[jp].y);
             Word2 la1 = prep2(ca[jp + 1].x), ha1 = prep2(ca[jp + 1].y), lb1 = prep2(cb[jp + 1].x), hb1 = prep2(cb[jp + 1].y);
-            const float4 cn0 = FMT == 1 ? lds128f(cbase + jp * 64) : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float4 cn1 = FMT == 1 ? lds128f(cbase + (jp + 1) * 64) : make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 cn0, cn1;                                      // 1-bit baselines (ternary: unused)
+            if (FMT == 1) {
+              cn0 = lds128f(cbase + jp * 64);
+              cn1 = lds128f(cbase + (jp + 1) * 64);
+            }
             uint4 bx0[4], bx1[4];
 #pragma unroll
             for (int iq = 0; iq < 4; ++iq) {
@@ -580,9 +638,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     const uint32_t e10 = areg<FMT, 2 * (I)>(w1a1, la1, ha1, M, SC), e11 = areg<FMT, 2 * (I)>(w1b1, lb1, hb1, M, SC);  \
     const uint32_t e12 = areg<FMT, 2 * (I) + 1>(w1a1, la1, ha1, M, SC);                                         \
     const uint32_t e13 = areg<FMT, 2 * (I) + 1>(w1b1, lb1, hb1, M, SC);                                         \
-    if ((I) == 0) {                                                                                        \
+    if ((I) == 0 && FMT == 1) {                                                                            \
       mma_c4(d0, e00, e01, e02, e03, b0lo, b0hi, cn0);                                                     \
       mma_c4(d1, e10, e11, e12, e13, b1lo, b1hi, cn1);                                                     \
+    } else if ((I) == 0) {                                                                                 \
+      mma_zero(d0, e00, e01, e02, e03, b0lo, b0hi);                                                        \
+      mma_zero(d1, e10, e11, e12, e13, b1lo, b1hi);                                                        \
     } else {                                                                                               \
       mma_acc(d0, e00, e01, e02, e03, b0lo, b0hi);                                                         \
       mma_acc(d1, e10, e11, e12, e13, b1lo, b1hi);                                                         \
@@ -604,7 +665,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 
       if (++cstage == nst) {
         cstage = 0;
-        // ---- row block done: the two halves meet in shared memory (double-buffered by row block)
+        // ---- row block done: the two halves of each tile meet in shared memory (double-buffered
+        // by row block); only the tile's two warps wait for each other
+        const int rb = unit_rb(i_rb);
+        const Prob& PU = a.p[unit_prob(i_rb)];                    // the matrix of this unit
         float* red = reinterpret_cast<float*>(sm + L::red) + (i_rb & 1) * ROWS * 8;
         if (half == 1) {
           red[ia * 8 + c0col] = acc[0];
@@ -613,14 +677,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
           red[(ia + 8) * 8 + c1col] = acc[3];
         }
         if (st == total_st - 1) griddep_launch();
-        consumer_sync();
+        tile_sync(tile);
         if (half == 0) {
+          const float f0 = colf[c0col] * mul, f1 = colf[c1col] * mul;   // output factors of my columns
           const float v0 = (acc[0] + red[ia * 8 + c0col]) * f0;
           const float v1 = (acc[1] + red[ia * 8 + c1col]) * f1;
           const float v2 = (acc[2] + red[(ia + 8) * 8 + c0col]) * f0;
           const float v3 = (acc[3] + red[(ia + 8) * 8 + c1col]) * f1;
           if (a.S == 1 && a.fuse && i_rb == 0) {
-            gate[0] = v0; gate[1] = v1; gate[2] = v2; gate[3] = v3;   // the gate unit: kept for the up unit
+            // the gate unit: its outputs wait in the first reduction buffer (which the up unit,
+            // using the second, leaves alone) where this thread reads them back
+            red[ia * 8 + c0col] = v0;
+            red[ia * 8 + c1col] = v1;
+            red[(ia + 8) * 8 + c0col] = v2;
+            red[(ia + 8) * 8 + c1col] = v3;
           } else if (a.S == 1) {
             const int row_a = rb * ROWS + ia, row_b = row_a + 8;
             auto put = [&](int row, int col, float v) {
@@ -628,10 +698,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                 PU.y[static_cast<int64_t>(col) * PU.n + row] =
                     XBF ? __bfloat16_as_ushort(__float2bfloat16_rn(v)) : __half_as_ushort(__float2half_rn(v));
             };
-            put(row_a, c0col, a.fuse ? silu(gate[0]) * v0 : v0);
-            put(row_a, c1col, a.fuse ? silu(gate[1]) * v1 : v1);
-            put(row_b, c0col, a.fuse ? silu(gate[2]) * v2 : v2);
-            put(row_b, c1col, a.fuse ? silu(gate[3]) * v3 : v3);
+            float o0 = v0, o1 = v1, o2 = v2, o3 = v3;
+            if (a.fuse) {                                          // the up unit: h = silu(g) * u
+              const float* g = reinterpret_cast<const float*>(sm + L::red);
+              o0 *= silu(g[ia * 8 + c0col]);
+              o1 *= silu(g[ia * 8 + c1col]);
+              o2 *= silu(g[(ia + 8) * 8 + c0col]);
+              o3 *= silu(g[(ia + 8) * 8 + c1col]);
+            }
+            put(row_a, c0col, o0);
+            put(row_a, c1col, o1);
+            put(row_b, c0col, o2);
+            put(row_b, c1col, o3);
           } else {
             red[ia * 8 + c0col] = v0;                              // this CTA's partial, in output units
             red[ia * 8 + c1col] = v1;
@@ -640,9 +718,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
           }
         }
         acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+        LB_TRACE(threadIdx.x == 0 && i_rb < 8, 21 + i_rb);
         ++i_rb;
       }
     }
+    LB_TRACE(threadIdx.x == 0, 29);
   }
 
   if (a.S > 1 && ng <= 0) {
@@ -678,6 +758,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     cluster_sync();
   }
   if (!ok) atomicOr(a.err, lb::kErrGemmTimeout);
+  LB_TRACE(threadIdx.x == 0, 30);
 }
 
 // ----------------------------------------------------------------------------- host side
@@ -1037,3 +1118,16 @@ lb_status launch_gemv_batched(const lb_gemv_problem* probs, int count, int xdt, 
 }
 
 }  // namespace lb
+
+#ifdef LB_GEMV_TRACE
+// Trace builds only: copy the phase trace (kTraceCtas x kTraceEvents x {globaltimer ns, clock64})
+// to host memory and clear it.  Returns the bytes copied, or -1 on a CUDA error.
+extern "C" long long lb_gemv_trace_read(void* host, long long bytes) {
+  const long long n = static_cast<long long>(sizeof(g_gemv_trace));
+  if (bytes < n) return -1;
+  if (cudaMemcpyFromSymbol(host, g_gemv_trace, sizeof(g_gemv_trace)) != cudaSuccess) return -1;
+  static unsigned long long zero[kTraceCtas][kTraceEvents][2];
+  if (cudaMemcpyToSymbol(g_gemv_trace, zero, sizeof(zero)) != cudaSuccess) return -1;
+  return n;
+}
+#endif

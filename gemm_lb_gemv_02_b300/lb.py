@@ -13,7 +13,8 @@ import ctypes
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "liblb.so")
+# LB_LIBRARY selects another build of the same library (the phase-trace build, see trace_gemv.py)
+LIB_PATH = os.environ.get("LB_LIBRARY") or os.path.join(HERE, "liblb.so")
 
 LB_OK = 0
 LB_FMT_1BIT_G128 = 1
