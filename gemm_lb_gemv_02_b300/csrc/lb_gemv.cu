@@ -173,12 +173,10 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-__device__ __forceinline__ float ld_dsmem(uint32_t local_addr, uint32_t rank) {
+__device__ __forceinline__ void st_dsmem(uint32_t local_addr, uint32_t rank, float v) {
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-  return v;
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 // Phase trace (compiled in only with -DLB_GEMV_TRACE, for timing studies): per CTA, event e holds
 // {%globaltimer, clock64} of the moment one fixed thread passed a point of the kernel.  Events:
@@ -271,7 +269,10 @@ struct Layout {
   static constexpr int bars = ring;                              // full[stages], empty[stages]
   static constexpr int red = bars + 128;                         // 2 x ROWS x 8 floats
   static constexpr int colf = red + 2 * ROWS * 8 * 4;            // 8 column factors + 8 column maxima
-  static constexpr int cneg = colf + 64;                         // gpc x 4 x float4 {-C[2q], -C[2q+1], same}
+  // K split across a cluster: rank p's partial of row r (unit u) lands in the row's owner at
+  // slot (u * S + p) * per + (r - owner's first row), per = ceil(ROWS / S) rows per owner
+  static constexpr int xchg = colf + 64;                         // 2 units x (ROWS + kMaxCluster) x 8 floats
+  static constexpr int cneg = xchg + 2 * (ROWS + kMaxCluster) * 8 * 4;   // gpc x 4 x float4 {-C[2q], -C[2q+1], same}
   static constexpr int xgroup = 4 * 4 * BP * 16;                 // x fragments of one group
   // the x fragments and baselines are padded to whole stages (zeros), so a stage is always full
   __host__ __device__ static int pad(int gpc) { return (gpc + GS - 1) / GS * GS; }
@@ -711,10 +712,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             put(row_b, c0col, o2);
             put(row_b, c1col, o3);
           } else {
-            red[ia * 8 + c0col] = v0;                              // this CTA's partial, in output units
-            red[ia * 8 + c1col] = v1;
-            red[(ia + 8) * 8 + c0col] = v2;
-            red[(ia + 8) * 8 + c1col] = v3;
+            // this CTA's partial, in output units, goes straight into the shared memory of the
+            // cluster CTA that owns the row (fire and forget; the cluster barrier after the loop
+            // makes it visible)
+            const int per = (ROWS + a.S - 1) / a.S;
+            const uint32_t xchg = sm32 + static_cast<uint32_t>(L::xchg);
+            auto push = [&](int lrow, int col, float v) {
+              if (col < a.batch) {
+                const int o = lrow / per;
+                const int slot_i = ((i_rb * a.S + static_cast<int>(rank)) * per + (lrow - o * per)) * 8 + col;
+                st_dsmem(xchg + static_cast<uint32_t>(slot_i * 4), static_cast<uint32_t>(o), v);
+              }
+            };
+            push(ia, c0col, v0);
+            push(ia, c1col, v1);
+            push(ia + 8, c0col, v2);
+            push(ia + 8, c1col, v3);
           }
         }
         acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
@@ -725,29 +738,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     LB_TRACE(threadIdx.x == 0, 29);
   }
 
-  if (a.S > 1 && ng <= 0) {
-    // a grouped launch splits every problem into S chunks; a short problem leaves some empty
-    float* red = reinterpret_cast<float*>(sm + L::red);
-    for (int i = threadIdx.x; i < (a.fuse ? 2 : 1) * ROWS * 8; i += kThreads) red[i] = 0.f;
-  }
   if (a.S > 1) {
-    // one row block per cluster: the S K-chunks' partial sums meet in distributed shared memory;
-    // every thread of every CTA (producer warp included) takes part in both cluster barriers
+    // one row block per cluster: every rank with a K chunk pushed its partials to the rows'
+    // owners; one cluster barrier (every thread of every CTA, producer warp included) and each
+    // owner sums its rows locally, in rank order.  No CTA touches another's shared memory after it.
     cluster_sync();
     if (warp < NW) {
       const int rb = rb0;
       const int per = (ROWS + a.S - 1) / a.S;
       const int lo = static_cast<int>(rank) * per, hi = min(ROWS, lo + per);
-      const uint32_t red = lbdev::smem_u32(sm + L::red);
+      const int nrank = min(a.S, (P.G + gpc - 1) / gpc);           // ranks that had groups
+      const float* xchg = reinterpret_cast<const float*>(sm + L::xchg);
       for (int e = threadIdx.x; e < (hi - lo) * a.batch; e += NW * 32) {
         const int lrow = lo + e / a.batch, col = e % a.batch;
         const int row = rb * ROWS + lrow;
         float v = 0.f;
-        for (int p = 0; p < a.S; ++p) v += ld_dsmem(red + (lrow * 8 + col) * 4, static_cast<uint32_t>(p));
+        for (int p = 0; p < nrank; ++p) v += xchg[(p * per + lrow - lo) * 8 + col];
         if (a.fuse) {                                              // v is the gate; the up partials follow
           float u = 0.f;
-          for (int p = 0; p < a.S; ++p)
-            u += ld_dsmem(red + (ROWS * 8 + lrow * 8 + col) * 4, static_cast<uint32_t>(p));
+          for (int p = 0; p < nrank; ++p) u += xchg[((a.S + p) * per + lrow - lo) * 8 + col];
           v = silu(v) * u;
         }
         if (row < P.n)
@@ -755,7 +764,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
               XBF ? __bfloat16_as_ushort(__float2bfloat16_rn(v)) : __half_as_ushort(__float2half_rn(v));
       }
     }
-    cluster_sync();
   }
   if (!ok) atomicOr(a.err, lb::kErrGemmTimeout);
   LB_TRACE(threadIdx.x == 0, 30);

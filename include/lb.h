@@ -150,8 +150,8 @@ lb_status lb_pack_ternary5(const int8_t* t, const uint16_t* s_in, int64_t n, int
  * batch : 1 .. 8.
  * Asynchronous on `stream`.  Errors (no launch): LB_ERR_NULL, LB_ERR_SHAPE, LB_ERR_ALIGN,
  * LB_ERR_DTYPE; LB_ERR_UNSUPPORTED if k is longer than 8 CTAs of a cluster hold in shared memory
- * (1-bit: k <= 352256 at batch 1, 196608 at batch 2, 98304 at batch 3-4, 49152 at batch 5-8;
- * ternary: k <= 376832, 204800, 106496, 49152); LB_ERR_CUDA if the launch fails.
+ * (1-bit: k <= 327680 at batch 1, 180224 at batch 2, 90112 at batch 3-4, 49152 at batch 5-8;
+ * ternary: k <= 344064, 188416, 98304, 49152); LB_ERR_CUDA if the launch fails.
  */
 lb_status lb_gemv(const lb_weight* W, const void* x, int xdt, int batch, void* y, lb_stream stream);
 

@@ -55,8 +55,8 @@ def _status(fn, *args):
 
 
 # The largest k lb_gemv takes per batch class (batch 1, 2, 3-4, 5-8), as include/lb.h states them.
-GEMV_K_LIMITS = {lb.LB_FMT_1BIT_G128: ((1, 352256), (2, 196608), (4, 98304), (8, 49152)),
-                 lb.LB_FMT_TERNARY_G128: ((1, 376832), (2, 204800), (4, 106496), (8, 49152))}
+GEMV_K_LIMITS = {lb.LB_FMT_1BIT_G128: ((1, 327680), (2, 180224), (4, 90112), (8, 49152)),
+                 lb.LB_FMT_TERNARY_G128: ((1, 344064), (2, 188416), (4, 98304), (8, 49152))}
 
 # Fake, never-dereferenced device addresses: validation must reject before any CUDA call.
 A16 = 0x10000

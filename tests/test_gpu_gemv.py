@@ -189,9 +189,9 @@ def test_gemv_batched_k_split_with_empty_chunks(fmt, batch):
         check_products(y, y_ref, a, f"batched split {fmt} n={n} k={k} batch={batch}")
 
 
-@pytest.mark.parametrize("fmt,batch,k", [("1bit", 1, 352256), ("1bit", 2, 196608), ("1bit", 4, 98304),
-                                         ("1bit", 8, 49152), ("ternary", 1, 376832), ("ternary", 2, 204800),
-                                         ("ternary", 4, 106496), ("ternary", 8, 49152)])
+@pytest.mark.parametrize("fmt,batch,k", [("1bit", 1, 327680), ("1bit", 2, 180224), ("1bit", 4, 90112),
+                                         ("1bit", 8, 49152), ("ternary", 1, 344064), ("ternary", 2, 188416),
+                                         ("ternary", 4, 98304), ("ternary", 8, 49152)])
 def test_gemv_at_k_limit(fmt, batch, k):
     """Each batch class at the largest K lb_gemv accepts (the K split then uses the widest
     cluster), with a ragged row count."""
