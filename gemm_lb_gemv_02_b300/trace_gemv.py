@@ -87,7 +87,7 @@ def summarize(tr: np.ndarray, clock_ghz: float) -> str:
     row("CTA start -> CTA end", kc(EV_START, EV_END), "kcyc")
     row("CTA end after the first CTA's start", (ns[:, EV_END] - t0) / 1e3, "us")
     lines.append("")
-    lines.append(f"(kcyc = 1000 SM cycles, {1 / clock_ghz:.3f} us at the {clock_ghz:.2f} GHz SM clock read at run time)")
+    lines.append(f"(kcyc = 1000 SM cycles, {1 / clock_ghz:.3f} us at the {clock_ghz:.2f} GHz maximum SM clock the device reports)")
     return "\n".join(lines) + "\n"
 
 
