@@ -500,12 +500,25 @@ def measure_swiglu_rows(lbt, peaks, sel=None):
                               for i in range(steps)])
         _time_graph(g_u)
         ms_u = _time_graph(g_u, reps=3) / steps
+        hc = torch.empty_like(h)
+
+        def unfused_combined(i):                    # grouped launch + the silu(g) * u combine kernel
+            lbt.gemv_batched([(pairs[i % copies][0], x), (pairs[i % copies][1], x)], [yg, yu])
+            torch.mul(torch.nn.functional.silu(yg), yu, out=hc)
+
+        g_c = _graph(lambda: [unfused_combined(i) for i in range(steps)])
+        _time_graph(g_c)
+        ms_c = _time_graph(g_c, reps=3) / steps
         by = per_copy - 2 * b * base[0].k - 2 * b * n     # x read once, one output vector
         gbs = by / (ms_f * 1e-3) / 1e9
         rows[name] = {"shape": [n, base[0].k], "fmt": wl.fmt, "batch": b, "us_per_pair": round(ms_f * 1e3, 2),
                       "GB_s": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 3),
-                      "unfused_grouped_us": round(ms_u * 1e3, 2), "copies_rotated": copies}
-        del pairs, g_f, g_u
+                      "unfused_grouped_us": round(ms_u * 1e3, 2),
+                      "unfused_grouped_plus_combine_us": round(ms_c * 1e3, 2),
+                      "note": "unfused: one grouped launch writing g and u; plus_combine adds the "
+                              "elementwise silu(g) * u (torch) the unfused path needs to produce h",
+                      "copies_rotated": copies}
+        del pairs, g_f, g_u, g_c
         torch.cuda.empty_cache()
     return rows
 
@@ -687,6 +700,8 @@ def run_ours(args, ws, rank, local):
     gs = GemvSet(wl, 1, lbt, copies=LAYERS, layers_per_step=LAYERS, grouping="layer")
     warm = _graph(lambda: [gs.step() for _ in range(max(1, args.warmup))])
     timed = _graph(lambda: [gs.step() for _ in range(args.steps)])
+    timed.replay()                    # a graph's first launch uploads it: keep that out of the timing
+    torch.cuda.synchronize()
     launches_per_layer = gs.launches_per_layer
     launches = args.steps * LAYERS * launches_per_layer
 
@@ -765,6 +780,7 @@ def run_ours(args, ws, rank, local):
         torch.cuda.current_stream().synchronize()
     e2e_graph_value = by_step / ((time.perf_counter() - t0) / e2e_steps) / 1e9
     del e2e_graph
+    e2e_c = run_e2e_c(LAYERS, e2e_steps, max(3, args.warmup))
 
     del gs, warm, timed
     torch.cuda.empty_cache()
@@ -812,13 +828,38 @@ def run_ours(args, ws, rank, local):
                        "again by this host-paced loop)",
                 "graph_value": round(e2e_graph_value, 1),
                 "graph_how": "the same copies and calls captured once into a CUDA graph, one replay + "
-                             "synchronize per step; host wall clock"},
+                             "synchronize per step; host wall clock",
+                "c_abi": e2e_c},
         "gpu_launches": launches,
         "clocks": clk,
         "peaks": peaks,
         "rows": rows,
     }
     print(json.dumps(line), flush=True)
+
+
+def run_e2e_c(layers: int, steps: int, warmup: int):
+    """The same end-to-end step from a plain C++ caller of the C ABI (gemm_lb_gemv_02_b300/e2e_c.cpp,
+    compiled here against liblb.so): its GB/s and the host microseconds spent inside each lb_* call."""
+    import subprocess
+    pkg = os.path.join(ROOT, "gemm_lb_gemv_02_b300")
+    src, exe = os.path.join(pkg, "e2e_c.cpp"), os.path.join(pkg, "_build", "e2e_c")
+    lib = os.path.join(pkg, "liblb.so")
+    try:
+        if not os.path.exists(exe) or os.path.getmtime(exe) < max(os.path.getmtime(src), os.path.getmtime(lib)):
+            os.makedirs(os.path.dirname(exe), exist_ok=True)
+            subprocess.run(["nvcc", "-O2", "-std=c++17", "-I", os.path.join(ROOT, "include"), "-o", exe, src,
+                            "-L" + pkg, "-llb", "-Xlinker", "-rpath=" + pkg], check=True, capture_output=True)
+        r = subprocess.run([exe, str(layers), str(steps), str(warmup)], capture_output=True, text=True, timeout=300)
+        if r.returncode != 0:
+            return {"unavailable": (r.stderr or r.stdout).strip()[-300:]}
+        out = json.loads(r.stdout.strip().splitlines()[-1])
+        out["how"] = ("e2e_c.cpp: the same step (pinned host x in, 4 calls per layer, outputs back, one "
+                      "stream synchronize) made by a C++ caller of include/lb.h; host wall clock; "
+                      "host_us_per_call = time inside the lb_* calls / calls")
+        return out
+    except Exception as e:                                    # the line still prints without it
+        return {"unavailable": f"{type(e).__name__}: {e}"[:300]}
 
 
 def run_rows_only(args, local):

@@ -565,10 +565,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     const float mul = FMT == 1 ? 2.f : 1.f;
     const int c0col = 2 * q, c1col = 2 * q + 1;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    int s = 0, cstage = 0, i_rb = 0;
+    int s = 0, st = 0;
     uint32_t ph = 0;
 
-    for (int st = 0; st < total_st; ++st) {
+    // units (row blocks) of this CTA; per unit nst stages of the ring, then the unit's epilogue
+    for (int i_rb = 0; i_rb < my_rbs; ++i_rb) {
+     for (int cstage = 0; cstage < nst; ++cstage, ++st) {
       const int g0 = cstage * GS + half * GH;                     // my first group, relative to g_begin
       const int cnt = min(GH, ng - g0);                           // my groups in this stage (may be <= 0)
       const uint32_t slot = sm32 + static_cast<uint32_t>(s * L::slot);
@@ -664,8 +666,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         }
       }
 
-      if (++cstage == nst) {
-        cstage = 0;
+     }
+      {
         // ---- row block done: the two halves of each tile meet in shared memory (double-buffered
         // by row block); only the tile's two warps wait for each other
         const int rb = unit_rb(i_rb);
@@ -677,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
           red[(ia + 8) * 8 + c0col] = acc[2];
           red[(ia + 8) * 8 + c1col] = acc[3];
         }
-        if (st == total_st - 1) griddep_launch();
+        if (i_rb == my_rbs - 1) griddep_launch();
         tile_sync(tile);
         if (half == 0) {
           const float f0 = colf[c0col] * mul, f1 = colf[c1col] * mul;   // output factors of my columns
@@ -732,7 +734,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         }
         acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
         LB_TRACE(threadIdx.x == 0 && i_rb < 8, 21 + i_rb);
-        ++i_rb;
       }
     }
     LB_TRACE(threadIdx.x == 0, 29);

@@ -39,6 +39,16 @@
  *     validation result, so their LB_OK means "done and valid".
  *   - Thread safety: every call may be made from any host thread; pack calls serialise on an
  *     internal mutex (they share one device-side validation word per device).
+ *   - Launch order: lb_gemv (1-bit and 2-bit ternary weights), lb_gemv_batched and lb_gemv_swiglu
+ *     are launched with programmatic dependent launch.  Such a launch may start while the kernel
+ *     enqueued just before it on `stream` is still running; it reads x and writes y only after
+ *     that kernel has completed, but it starts streaming the packed weights (codes and scales)
+ *     before.  The weights must therefore not be written by the kernel that immediately precedes
+ *     the call on `stream`: write them at least one kernel earlier, or separate the two by a host
+ *     synchronisation.  The pack calls synchronise, so packing and then multiplying is safe.
+ *     Activations and outputs carry no such restriction (x may come from the preceding kernel, y
+ *     may be read by the next one).  lb_gemm, lb_gemm_noalloc, lb_embed and the five-per-byte
+ *     GEMV wait for the preceding kernel before reading anything.
  */
 #ifndef LB_H_
 #define LB_H_
