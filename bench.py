@@ -358,7 +358,9 @@ GEMM_ROWS = (
     # name, workload, matrix index, tokens
     ("gemm_c5", "c5", 0, 512),
     ("gemm_c4b_1bit_gate", "c4b", 2, 512),
+    ("gemm_c5_m8", "c5", 0, 8),
     ("gemm_c5_m16", "c5", 0, 16),
+    ("gemm_c5_m32", "c5", 0, 32),
     ("gemm_c5_m64", "c5", 0, 64),
     ("gemm_c5_m128", "c5", 0, 128),
 )

@@ -623,7 +623,10 @@ lb_status gemm_maps(const lb_weight& W, int scales_tma, CUtensorMap& tm_codes, C
 // padded token row.
 size_t gemm_workspace_bytes(int64_t m, int64_t k) {
   const int64_t mpad = (m + BM - 1) / BM * BM;
-  return static_cast<size_t>(mpad) * (static_cast<size_t>(k) * 2 + 4);
+  const size_t tiles = static_cast<size_t>(mpad) * (static_cast<size_t>(k) * 2 + 4);
+  if (m > kGemmSmallM) return tiles;
+  const size_t small = gemm_ms_workspace_bytes(m, k);              // the small-M path's staging
+  return small > tiles ? small : tiles;
 }
 
 lb_status launch_gemm(const lb_weight& W, const void* x, int xdt, int64_t m, void* y, int ydt, void* ws,
@@ -638,6 +641,8 @@ lb_status launch_gemm(const lb_weight& W, const void* x, int xdt, int64_t m, voi
   CUtensorMap tm_codes, tm_scales;
   lb_status ms = gemm_maps(W, scales_tma, tm_codes, tm_scales);
   if (ms != LB_OK) return ms;
+  if (m <= kGemmSmallM)                                            // few tokens: the decode dominates
+    return launch_gemm_ms(W, x, xdt, m, y, ydt, ws, tm_codes, tm_scales, scales_tma, fault, st);
   const uint16_t* xs = static_cast<const uint16_t*>(x);
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   float* fac = reinterpret_cast<float*>(wsb + static_cast<size_t>(mpad) * static_cast<size_t>(k) * 2);

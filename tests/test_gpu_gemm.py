@@ -133,3 +133,20 @@ def test_gemm_long_k(fmt):
     pw, codes, scales = _packed(fmt, n, k, seed=92)
     x = synth.activations(m, k, "bf16", seed=93)
     _check(pw, codes, scales, x, torch.bfloat16, f"gemm {fmt} k={k}")
+
+
+@pytest.mark.parametrize("fmt,m", [("ternary", 8), ("ternary", 16), ("ternary", 32), ("1bit", 12), ("1bit", 32)])
+def test_gemm_small_m_block_matrix(fmt, m):
+    """The few-token path (verification width, short prefill chunks) on a 17408 x 5120 block
+    matrix: every token row, first / last and 1500 sampled weight rows."""
+    key = "c5" if fmt == "ternary" else "c4b"
+    wl = synth.WORKLOADS[key]
+    idx = next(i for i, mt in enumerate(wl.matrices) if mt.n == 17408)
+    mat = wl.matrices[idx]
+    inp = synth.matrix_inputs(wl, idx)
+    pw = tensors.pack_1bit(inp["w"].cuda()) if fmt == "1bit" else tensors.pack_ternary(inp["t"].cuda(), inp["s"].cuda())
+    x = synth.workload_activations(wl, idx, m)
+    codes, scales = oracle_pack(fmt, inp)
+    rng = np.random.default_rng(7 + m)
+    cols = np.unique(np.concatenate([np.arange(8), np.arange(mat.n - 8, mat.n), rng.integers(0, mat.n, 1500)]))
+    _check(pw, codes, scales, x, torch.bfloat16, f"{key} m={m}", cols=cols)

@@ -75,8 +75,9 @@ def test_gemv_batched_wait_gives_up_then_recovers():
 
 
 @pytest.mark.parametrize("fmt", ["1bit", "ternary"])
-def test_gemm_wait_gives_up_then_recovers(fmt):
-    n, k, m = 256, 1024, 40
+@pytest.mark.parametrize("m", [40, 16])                       # the tensor-memory path; the few-token path
+def test_gemm_wait_gives_up_then_recovers(fmt, m):
+    n, k = 256, 1024
     pw, codes, scales = _packed(fmt, n, k, seed=3)
     x = synth.activations(m, k, "bf16", seed=4)
     assert lb.lb_device_error(clear=True) == 0
