@@ -153,8 +153,11 @@ struct Args {
   uint64_t wait_ns;
 };
 
+// BP = 0 selects the 1-bit lookup-table consumer at batch 1 (see the kernel): its x region is a
+// table of 2 KB per group instead of mma.sync fragments, and it has no baselines.
 template <int FMT, int BP>
 struct Layout {
+  static constexpr bool LU = BP == 0;
   static constexpr int stages = FmtTraits<FMT>::stages;
   static constexpr int slot = FmtTraits<FMT>::nb * kBox + kScaleBox;
   static constexpr int ring = stages * slot;                     // 1024-byte aligned base
@@ -165,10 +168,11 @@ struct Layout {
   // slot (u * S + p) * per + (r - owner's first row), per = ceil(ROWS / S) rows per owner
   static constexpr int xchg = colf + 64;                         // 2 units x (ROWS + kMaxCluster) x 8 floats
   static constexpr int cneg = xchg + 2 * (ROWS + kMaxCluster) * 8 * 4;   // gpc x 4 x float4 {-C[2q], -C[2q+1], same}
-  static constexpr int xgroup = 4 * 4 * BP * 16;                 // x fragments of one group
-  // the x fragments and baselines are padded to whole stages (zeros), so a stage is always full
+  static constexpr int xgroup = LU ? 32 * 16 * 4 : 4 * 4 * BP * 16;   // x fragments (table) of one group
+  // the x fragments and baselines are padded to whole stages (zeros), so a stage is always full;
+  // the table starts on a 256-byte boundary (its lookups replace an address's low byte)
   __host__ __device__ static int pad(int gpc) { return (gpc + GS - 1) / GS * GS; }
-  __host__ __device__ static int xs(int gpc) { return cneg + pad(gpc) * 64; }
+  __host__ __device__ static int xs(int gpc) { return LU ? (cneg + 255) / 256 * 256 : cneg + pad(gpc) * 64; }
   // + 512 bytes that lanes outside the batch may read past the last group, + 1024 alignment slack
   __host__ __device__ static int total(int gpc) { return xs(gpc) + pad(gpc) * xgroup + 512 + 1024; }
 };
@@ -292,6 +296,140 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     }
     __syncwarp();
     griddep_launch();
+  } else if constexpr (L::LU) {
+    // ======================= consumers, 1-bit lookup-table form (batch 1).  Per chunk of four
+    // activations the table holds the 16 signed sums sum_i (b_i ? +x_i : -x_i) (FP32, in the
+    // chunk's 64 bytes), so a code nibble b_0..b_3 costs one lookup and one add: thread = weight row,
+    // warp = 32 rows x 2 of a stage's 8 groups; four warps share rows and add up at the row block's
+    // end.  bfloat16 x is scaled by the same exact power of two as the fragment form (column max in
+    // [2^15, 2^16)) and the result scaled back.
+    float* colf = reinterpret_cast<float*>(sm + L::colf);
+    float* tab = reinterpret_cast<float*>(sm + L::xs(gpc));
+    griddep_wait();                                   // x is read and y written only after this
+    LB_TRACE(threadIdx.x == 0, 3);
+    const int chunks = ng > 0 ? ng * 32 : 0;
+    const uint16_t* xrow = P.x + static_cast<int64_t>(g_begin) * 128;
+    float scale = 1.f;
+    if (XBF) {
+      uint32_t mx = 0;
+      for (int c = threadIdx.x; c < chunks; c += NW * 32) {
+        const uint2 v = __ldg(reinterpret_cast<const uint2*>(xrow) + c);
+        mx = max(mx, max(max((v.x << 16) & 0x7f800000u, v.x & 0x7f800000u),
+                         max((v.y << 16) & 0x7f800000u, v.y & 0x7f800000u)));
+      }
+      for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      if (lane == 0) atomicMax(reinterpret_cast<uint32_t*>(colf + 8), mx);
+      consumer_sync();
+      const int e = static_cast<int>(reinterpret_cast<uint32_t*>(colf + 8)[0] >> 23) - 127;
+      const int p = max(-126, min(126, 15 - e));
+      scale = __uint_as_float(static_cast<uint32_t>(127 + p) << 23);
+      if (threadIdx.x == 0) colf[0] = __uint_as_float(static_cast<uint32_t>(127 - p) << 23);
+    } else if (threadIdx.x == 0) {
+      colf[0] = 1.f;
+    }
+    for (int c = threadIdx.x; c < L::pad(ng > 0 ? ng : 0) * 32; c += NW * 32) {
+      float v[4] = {0.f, 0.f, 0.f, 0.f};                          // padding chunks: all-zero sums
+      if (c < chunks) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(xrow) + c);
+        if (XBF) {
+          v[0] = __uint_as_float(u.x << 16) * scale; v[1] = __uint_as_float(u.x & 0xffff0000u) * scale;
+          v[2] = __uint_as_float(u.y << 16) * scale; v[3] = __uint_as_float(u.y & 0xffff0000u) * scale;
+        } else {
+          const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+          const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+          v[0] = lo.x; v[1] = lo.y; v[2] = hi.x; v[3] = hi.y;
+        }
+      }
+      const float lo4[4] = {-v[0] - v[1], v[0] - v[1], v[1] - v[0], v[0] + v[1]};   // bits 0, 1
+      const float hi4[4] = {-v[2] - v[3], v[2] - v[3], v[3] - v[2], v[2] + v[3]};   // bits 2, 3
+      float4* dst = reinterpret_cast<float4*>(tab + c * 16);
+#pragma unroll
+      for (int h = 0; h < 4; ++h)
+        dst[h] = make_float4(lo4[0] + hi4[h], lo4[1] + hi4[h], lo4[2] + hi4[h], lo4[3] + hi4[h]);
+    }
+    consumer_sync();
+    LB_TRACE(threadIdx.x == 0, 4);
+
+    const int rq = warp & 3, kq = warp >> 2;                      // rows 32 rq .., groups 2 kq, 2 kq + 1
+    const int row_l = 32 * rq + lane;
+    const uint32_t sm32 = lbdev::smem_u32(sm);
+    const uint32_t tb = sm32 + static_cast<uint32_t>(L::xs(gpc));   // 256-byte aligned
+    const uint32_t code0 = static_cast<uint32_t>(row_l * 128 + (((2 * kq) ^ (row_l & 7)) << 4));
+    const uint32_t code1 = static_cast<uint32_t>(row_l * 128 + (((2 * kq + 1) ^ (row_l & 7)) << 4));
+    const uint32_t sc_off = static_cast<uint32_t>(kBox + row_l * 16 + 4 * kq);
+    float acc = 0.f;
+    int s = 0, st = 0;
+    uint32_t ph = 0;
+    for (int i_rb = 0; i_rb < my_rbs; ++i_rb) {
+      for (int cstage = 0; cstage < nst; ++cstage, ++st) {
+        const uint32_t slot = sm32 + static_cast<uint32_t>(s * L::slot);
+        if (ok && !lbdev::mbar_wait(&full[s], ph, a.wait_ns)) ok = false;
+        ok = __all_sync(0xffffffffu, ok);
+        LB_TRACE(threadIdx.x == 0 && st < 16, 5 + st);
+        uint4 w[2];
+        uint32_t sc2 = 0;
+        if (ok) {
+          w[0] = ldsv128(slot + code0);
+          w[1] = ldsv128(slot + code1);
+          sc2 = ldsv32(slot + sc_off);
+        }
+        __syncwarp();
+        if (lane == 0) lbdev::mbar_arrive(&empty[s]);             // slot s released by this warp
+        if (++s == L::stages) { s = 0; ph ^= 1u; }
+        if (ok && cstage * GS + 2 * kq < ng) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            // the chunk of nibble j of word u is 8u + j of the group: low byte (j % 4) * 64 + 4 * idx,
+            // (j / 4) * 256 and u * 512 as offsets from the group's 2 KB
+            const uint32_t base = tb + static_cast<uint32_t>((cstage * GS + 2 * kq + h) * 2048);
+            float p4[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint32_t wd[4] = {w[h].x, w[h].y, w[h].z, w[h].w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              uint32_t ev, od;
+              asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(ev) : "r"(wd[u] << 2), "r"(0x3C3C3C3Cu), "r"(0x80008000u));
+              asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(od) : "r"(wd[u] >> 2), "r"(0x3C3C3C3Cu), "r"(0xC040C040u));
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const uint32_t ad = __byte_perm((j & 1) ? od : ev, base, 0x7650 | (j >> 1));
+                float t;
+                asm("ld.shared.f32 %0, [%1];" : "=f"(t) : "r"(ad + u * 512 + (j >> 2) * 256));
+                p4[j & 3] += t;
+              }
+            }
+            const float sg = __half2float(__ushort_as_half(static_cast<unsigned short>(sc2 >> (16 * h))));
+            acc = fmaf(sg, (p4[0] + p4[1]) + (p4[2] + p4[3]), acc);
+          }
+        }
+      }
+      // ---- row block done: the four K quarters of each row meet in shared memory
+      const int rb = unit_rb(i_rb);
+      const Prob& PU = a.p[unit_prob(i_rb)];
+      float* red = reinterpret_cast<float*>(sm + L::red) + (i_rb & 1) * ROWS * 8;
+      if (kq != 0) red[kq * ROWS + row_l] = acc;
+      if (i_rb == my_rbs - 1) griddep_launch();
+      asm volatile("bar.sync %0, 128;" ::"r"(2 + rq) : "memory");
+      if (kq == 0) {
+        const float v = (acc + red[ROWS + row_l] + red[2 * ROWS + row_l] + red[3 * ROWS + row_l]) * colf[0];
+        float* gate = reinterpret_cast<float*>(sm + L::red);      // the gate unit's outputs (fused pair)
+        if (a.S == 1 && a.fuse && i_rb == 0) {
+          gate[row_l] = v;
+        } else if (a.S == 1) {
+          const int row = rb * ROWS + row_l;
+          const float o = a.fuse ? v * silu(gate[row_l]) : v;
+          if (row < PU.n)
+            PU.y[row] = XBF ? __bfloat16_as_ushort(__float2bfloat16_rn(o)) : __half_as_ushort(__float2half_rn(o));
+        } else {
+          const int per = (ROWS + a.S - 1) / a.S;
+          const int o = row_l / per;
+          const int slot_i = ((i_rb * a.S + static_cast<int>(rank)) * per + (row_l - o * per)) * 8;
+          st_dsmem(sm32 + static_cast<uint32_t>(L::xchg + slot_i * 4), static_cast<uint32_t>(o), v);
+        }
+      }
+      acc = 0.f;
+      LB_TRACE(threadIdx.x == 0 && i_rb < 8, 21 + i_rb);
+    }
+    LB_TRACE(threadIdx.x == 0, 29);
   } else {
     // ======================= consumers
     const int r = lane >> 2, q = lane & 3;
@@ -674,7 +812,7 @@ struct Plan {
 template <int FMT, int BP>
 Plan plan_split(int G, int row_blocks, int sms) {
   using L = Layout<FMT, BP>;
-  const double t_group = 16384.0 * (FmtTraits<FMT>::gbytes + 2) / 128.0 / 40.0;   // ns per 128x128 tile
+  const double t_group = (L::LU ? 0.5 : 1.0) * 16384.0 * (FmtTraits<FMT>::gbytes + 2) / 128.0 / 40.0;   // ns per 128x128 tile
   Plan best{0, 0};
   double best_t = 1e30;
   for (int s_try = 1; s_try <= kMaxCluster; ++s_try) {
@@ -855,7 +993,7 @@ lb_status launch_many(const lb_gemv_problem* probs, int count, int batch, cudaSt
       order[j - 1] = t;
     }
   const int sms = lb::sm_count();
-  const double t_group = 16384.0 * (FmtTraits<FMT>::gbytes + 2) / 128.0 / 40.0;   // ns per 128x128 tile
+  const double t_group = (L::LU ? 0.5 : 1.0) * 16384.0 * (FmtTraits<FMT>::gbytes + 2) / 128.0 / 40.0;   // ns per 128x128 tile
   int units = 0, gmax = 0;
   for (int i = 0; i < count; ++i) {
     units += static_cast<int>((probs[i].W.n + ROWS - 1) / ROWS);
@@ -914,7 +1052,7 @@ lb_status launch_pair(const lb_weight& Wg, const lb_weight& Wu, const uint16_t* 
                       cudaStream_t st) {
   using L = Layout<FMT, BP>;
   const int sms = lb::sm_count();
-  const double t_group = 16384.0 * (FmtTraits<FMT>::gbytes + 2) / 128.0 / 40.0;   // ns per 128x128 tile
+  const double t_group = (L::LU ? 0.5 : 1.0) * 16384.0 * (FmtTraits<FMT>::gbytes + 2) / 128.0 / 40.0;   // ns per 128x128 tile
   const int G = static_cast<int>(Wg.k / lb::kGroup);
   const int units = static_cast<int>((Wg.n + ROWS - 1) / ROWS);
   auto chunk = [](int g, int S) { return S == 1 ? g : ((g + S - 1) / S + GS - 1) / GS * GS; };
@@ -945,10 +1083,19 @@ lb_status launch_pair(const lb_weight& Wg, const lb_weight& Wu, const uint16_t* 
   return launch_args<FMT, XBF, BP>(args, best_s, units, L::total(gpc), st);
 }
 
+// 1-bit at batch 1 takes the lookup-table consumer (BP = 0) whenever its table fits.
+template <int FMT>
+bool lut_fits(int G, int row_blocks) {
+  return FMT == 1 && plan_split<FMT, 0>(G, row_blocks, lb::sm_count()).S != 0;
+}
 template <int FMT, bool XBF>
 lb_status launch_b(const lb_weight& W, const uint16_t* x, int batch, uint16_t* y, cudaStream_t st) {
   switch (pad_batch(batch)) {
-    case 1: return launch_t<FMT, XBF, 1>(W, x, batch, y, st);
+    case 1:
+      if constexpr (FMT == 1)
+        if (lut_fits<FMT>(static_cast<int>(W.k / lb::kGroup), static_cast<int>((W.n + ROWS - 1) / ROWS)))
+          return launch_t<FMT, XBF, 0>(W, x, batch, y, st);
+      return launch_t<FMT, XBF, 1>(W, x, batch, y, st);
     case 2: return launch_t<FMT, XBF, 2>(W, x, batch, y, st);
     case 4: return launch_t<FMT, XBF, 4>(W, x, batch, y, st);
     default: return launch_t<FMT, XBF, 8>(W, x, batch, y, st);
@@ -958,7 +1105,11 @@ template <int FMT, bool XBF>
 lb_status launch_pb(const lb_weight& Wg, const lb_weight& Wu, const uint16_t* x, int batch, uint16_t* h,
                     cudaStream_t st) {
   switch (pad_batch(batch)) {
-    case 1: return launch_pair<FMT, XBF, 1>(Wg, Wu, x, batch, h, st);
+    case 1:
+      if constexpr (FMT == 1)
+        if (lut_fits<FMT>(static_cast<int>(Wg.k / lb::kGroup), static_cast<int>((Wg.n + ROWS - 1) / ROWS)))
+          return launch_pair<FMT, XBF, 0>(Wg, Wu, x, batch, h, st);
+      return launch_pair<FMT, XBF, 1>(Wg, Wu, x, batch, h, st);
     case 2: return launch_pair<FMT, XBF, 2>(Wg, Wu, x, batch, h, st);
     case 4: return launch_pair<FMT, XBF, 4>(Wg, Wu, x, batch, h, st);
     default: return launch_pair<FMT, XBF, 8>(Wg, Wu, x, batch, h, st);
@@ -967,7 +1118,16 @@ lb_status launch_pb(const lb_weight& Wg, const lb_weight& Wu, const uint16_t* x,
 template <int FMT, bool XBF>
 lb_status launch_mb(const lb_gemv_problem* probs, int count, int batch, cudaStream_t st) {
   switch (pad_batch(batch)) {
-    case 1: return launch_many<FMT, XBF, 1>(probs, count, batch, st);
+    case 1:
+      if constexpr (FMT == 1) {
+        int gmax = 0, units = 0;
+        for (int i = 0; i < count; ++i) {
+          gmax = max(gmax, static_cast<int>(probs[i].W.k / lb::kGroup));
+          units += static_cast<int>((probs[i].W.n + ROWS - 1) / ROWS);
+        }
+        if (lut_fits<FMT>(gmax, units)) return launch_many<FMT, XBF, 0>(probs, count, batch, st);
+      }
+      return launch_many<FMT, XBF, 1>(probs, count, batch, st);
     case 2: return launch_many<FMT, XBF, 2>(probs, count, batch, st);
     case 4: return launch_many<FMT, XBF, 4>(probs, count, batch, st);
     default: return launch_many<FMT, XBF, 8>(probs, count, batch, st);
