@@ -309,43 +309,50 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     LB_TRACE(threadIdx.x == 0, 3);
     const int chunks = ng > 0 ? ng * 32 : 0;
     const uint16_t* xrow = P.x + static_cast<int64_t>(g_begin) * 128;
-    float scale = 1.f;
-    if (XBF) {
+    // item t = (chunk c, quarter h): the four entries 4h .. 4h + 3 of chunk c, so that a warp's
+    // 16-byte stores are contiguous (no bank conflicts).  The entries are FP32 sums of the exact
+    // activations, built in one pass; bfloat16 columns whose largest magnitude is 2^100 or more
+    // (where sums of four could overflow) are built again scaled down by a power of two.
+    const int items = L::pad(ng > 0 ? ng : 0) * 32 * 4;
+    auto build = [&](float scale) -> uint32_t {
       uint32_t mx = 0;
-      for (int c = threadIdx.x; c < chunks; c += NW * 32) {
-        const uint2 v = __ldg(reinterpret_cast<const uint2*>(xrow) + c);
-        mx = max(mx, max(max((v.x << 16) & 0x7f800000u, v.x & 0x7f800000u),
-                         max((v.y << 16) & 0x7f800000u, v.y & 0x7f800000u)));
+#pragma unroll 4
+      for (int t = threadIdx.x; t < items; t += NW * 32) {
+        const int c = t >> 2, h = t & 3;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};                        // padding chunks: all-zero sums
+        if (c < chunks) {
+          const uint2 u = __ldg(reinterpret_cast<const uint2*>(xrow) + c);
+          if (XBF) {
+            mx = max(mx, max(max((u.x << 16) & 0x7f800000u, u.x & 0x7f800000u),
+                             max((u.y << 16) & 0x7f800000u, u.y & 0x7f800000u)));
+            v[0] = __uint_as_float(u.x << 16) * scale; v[1] = __uint_as_float(u.x & 0xffff0000u) * scale;
+            v[2] = __uint_as_float(u.y << 16) * scale; v[3] = __uint_as_float(u.y & 0xffff0000u) * scale;
+          } else {
+            const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+            const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+            v[0] = lo.x; v[1] = lo.y; v[2] = hi.x; v[3] = hi.y;
+          }
+        }
+        const float lo4[4] = {-v[0] - v[1], v[0] - v[1], v[1] - v[0], v[0] + v[1]};   // bits 0, 1
+        const float hi = ((h & 1) ? v[2] : -v[2]) + ((h & 2) ? v[3] : -v[3]);         // bits 2, 3 = h
+        reinterpret_cast<float4*>(tab)[t] = make_float4(lo4[0] + hi, lo4[1] + hi, lo4[2] + hi, lo4[3] + hi);
       }
+      return mx;
+    };
+    uint32_t mx = build(1.f);
+    if (XBF) {
       for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       if (lane == 0) atomicMax(reinterpret_cast<uint32_t*>(colf + 8), mx);
-      consumer_sync();
-      const int e = static_cast<int>(reinterpret_cast<uint32_t*>(colf + 8)[0] >> 23) - 127;
-      const int p = max(-126, min(126, 15 - e));
-      scale = __uint_as_float(static_cast<uint32_t>(127 + p) << 23);
+    }
+    consumer_sync();
+    const int e = XBF ? static_cast<int>(reinterpret_cast<uint32_t*>(colf + 8)[0] >> 23) - 127 : 0;
+    if (e >= 100) {                                                 // block-uniform
+      const int p = 99 - e;                                         // largest magnitude below 2^100
+      build(__uint_as_float(static_cast<uint32_t>(127 + p) << 23));
       if (threadIdx.x == 0) colf[0] = __uint_as_float(static_cast<uint32_t>(127 - p) << 23);
+      consumer_sync();
     } else if (threadIdx.x == 0) {
       colf[0] = 1.f;
-    }
-    for (int c = threadIdx.x; c < L::pad(ng > 0 ? ng : 0) * 32; c += NW * 32) {
-      float v[4] = {0.f, 0.f, 0.f, 0.f};                          // padding chunks: all-zero sums
-      if (c < chunks) {
-        const uint2 u = __ldg(reinterpret_cast<const uint2*>(xrow) + c);
-        if (XBF) {
-          v[0] = __uint_as_float(u.x << 16) * scale; v[1] = __uint_as_float(u.x & 0xffff0000u) * scale;
-          v[2] = __uint_as_float(u.y << 16) * scale; v[3] = __uint_as_float(u.y & 0xffff0000u) * scale;
-        } else {
-          const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-          const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-          v[0] = lo.x; v[1] = lo.y; v[2] = hi.x; v[3] = hi.y;
-        }
-      }
-      const float lo4[4] = {-v[0] - v[1], v[0] - v[1], v[1] - v[0], v[0] + v[1]};   // bits 0, 1
-      const float hi4[4] = {-v[2] - v[3], v[2] - v[3], v[3] - v[2], v[2] + v[3]};   // bits 2, 3
-      float4* dst = reinterpret_cast<float4*>(tab + c * 16);
-#pragma unroll
-      for (int h = 0; h < 4; ++h)
-        dst[h] = make_float4(lo4[0] + hi4[h], lo4[1] + hi4[h], lo4[2] + hi4[h], lo4[3] + hi4[h]);
     }
     consumer_sync();
     LB_TRACE(threadIdx.x == 0, 4);

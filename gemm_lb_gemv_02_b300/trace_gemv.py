@@ -93,7 +93,7 @@ def summarize(tr: np.ndarray, clock_ghz: float) -> str:
 
 def main() -> None:
     ap = argparse.ArgumentParser()
-    ap.add_argument("--workload", default="c4t", choices=sorted(LAYERS))
+    ap.add_argument("--workload", default="c4t", help="a layer workload (c2, c4t, c4b) or a single-matrix one (c1, c3)")
     ap.add_argument("--launch", type=int, default=2, help="index of the traced launch in the layer")
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--warmup", type=int, default=5)
@@ -118,7 +118,8 @@ def main() -> None:
         inp = synth.matrix_inputs(wl, i)
         packed.append(tensors.pack_1bit(inp["w"].cuda()) if wl.fmt == "1bit"
                       else tensors.pack_ternary(inp["t"].cuda(), inp["s"].cuda()))
-    groups = [[names.index(n) for n in g] for g in LAYERS[a.workload]]
+    layers = LAYERS.get(a.workload, [[n] for n in names])
+    groups = [[names.index(n) for n in g] for g in layers]
     xs = {g[0]: synth.workload_activations(wl, g[0], a.batch).cuda() for g in groups}
     if a.xdtype:
         xs = {i: x.to(torch.bfloat16 if a.xdtype == "bf16" else torch.float16) for i, x in xs.items()}
@@ -143,7 +144,7 @@ def main() -> None:
     clock_ghz = torch.cuda.get_device_properties(0).clock_rate / 1e6 if hasattr(
         torch.cuda.get_device_properties(0), "clock_rate") else 1.92
     print(f"## GEMV phase trace: {a.workload}, launch {a.launch} "
-          f"({'+'.join(LAYERS[a.workload][a.launch])}), batch {a.batch}, x {next(iter(xs.values())).dtype}\n")
+          f"({'+'.join(layers[a.launch])}), batch {a.batch}, x {next(iter(xs.values())).dtype}\n")
     print(summarize(buf, clock_ghz))
 
 
