@@ -220,7 +220,7 @@ lb_status lb_gemv(const lb_weight* W, const void* x, int xdt, int batch, void* y
   if (!valid_dtype(xdt)) return fail(LB_ERR_DTYPE, "unknown activation dtype %d", xdt);
   if (batch < 1 || batch > 8) return fail(LB_ERR_SHAPE, "batch must be in [1, 8] (got %d)", batch);
   if (!lb::aligned16(x) || !lb::aligned16(y)) return fail(LB_ERR_ALIGN, "x and y must be 16-byte aligned");
-  if (W->fmt == LB_FMT_TERNARY5_G128)
+  if (W->fmt == LB_FMT_TERNARY5_G128 && !lb::gemv_t5_lut_ok(*W, batch))
     return lb::launch_gemv_t5(*W, x, xdt, batch, y, reinterpret_cast<cudaStream_t>(stream));
   return lb::launch_gemv(*W, x, xdt, batch, y, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -55,6 +55,9 @@ lb_status launch_pack_1bit(const float* w, int64_t n, int64_t k, uint8_t* codes,
 lb_status launch_pack_ternary(const int8_t* t, const uint16_t* s_in, int64_t n, int64_t k,
                               uint8_t* codes, uint16_t* scales, cudaStream_t st, uint32_t* flags_out);
 lb_status launch_gemv(const lb_weight& W, const void* x, int xdt, int batch, void* y, cudaStream_t st);
+// Whether launch_gemv takes a five-per-byte weight (batch 1, lookup tables); otherwise
+// launch_gemv_t5 (CUDA cores) does.
+bool gemv_t5_lut_ok(const lb_weight& W, int batch);
 // The GEMM of 1 .. 32 token rows on the GEMV's mma.sync engine (lb_gemm_ms.cu); lb_gemm dispatches
 // to it.  The tensor maps are lb_gemm's (codes: 128 x 128-row boxes, 128-byte swizzle; scales:
 // 8 x 128-row boxes).

@@ -72,10 +72,17 @@ struct FmtTraits;
 template <>
 struct FmtTraits<1> {                     // 1-bit: 16 B per group per row, 8 groups per box
   static constexpr int gbytes = 16, nb = 1, stages = 6;
+  static constexpr int box = kBox;
 };
 template <>
 struct FmtTraits<2> {                     // ternary: 32 B per group per row, 4 groups per box
   static constexpr int gbytes = 32, nb = 2, stages = 3;
+  static constexpr int box = kBox;
+};
+template <>
+struct FmtTraits<3> {                     // ternary five per byte: 26 B per group per row, one
+  static constexpr int gbytes = 26, nb = 1, stages = 2;   // 128-row x 208-byte box (no swizzle)
+  static constexpr int box = 8 * 26 * 128;
 };
 
 // SiLU gate, silu(g) = g * sigmoid(g) = g / (1 + e^-g), in FP32 (expf: CUDA's accurate
@@ -159,7 +166,7 @@ template <int FMT, int BP>
 struct Layout {
   static constexpr bool LU = BP == 0;
   static constexpr int stages = FmtTraits<FMT>::stages;
-  static constexpr int slot = FmtTraits<FMT>::nb * kBox + kScaleBox;
+  static constexpr int slot = FmtTraits<FMT>::nb * FmtTraits<FMT>::box + kScaleBox;
   static constexpr int ring = stages * slot;                     // 1024-byte aligned base
   static constexpr int bars = ring;                              // full[stages], empty[stages]
   static constexpr int red = bars + 128;                         // 2 x ROWS x 8 floats
@@ -168,7 +175,7 @@ struct Layout {
   // slot (u * S + p) * per + (r - owner's first row), per = ceil(ROWS / S) rows per owner
   static constexpr int xchg = colf + 64;                         // 2 units x (ROWS + kMaxCluster) x 8 floats
   static constexpr int cneg = xchg + 2 * (ROWS + kMaxCluster) * 8 * 4;   // gpc x 4 x float4 {-C[2q], -C[2q+1], same}
-  static constexpr int xgroup = LU ? 32 * 16 * 4 : 4 * 4 * BP * 16;   // x fragments (table) of one group
+  static constexpr int xgroup = LU ? (FMT == 3 ? 26 * 36 * 4 : 32 * 16 * 4) : 4 * 4 * BP * 16;   // x fragments (table) of one group
   // the x fragments and baselines are padded to whole stages (zeros), so a stage is always full;
   // the table starts on a 256-byte boundary (its lookups replace an address's low byte)
   __host__ __device__ static int pad(int gpc) { return (gpc + GS - 1) / GS * GS; }
@@ -253,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
           lbdev::prefetch_tmap(&a.p[i].tm_codes);
           if (stma) lbdev::prefetch_tmap(&a.p[i].tm_scales);
         }
-    const uint32_t bytes = static_cast<uint32_t>(FT::nb * kBox + (stma ? kScaleBox : 0));
+    const uint32_t bytes = static_cast<uint32_t>(FT::nb * FT::box + (stma ? kScaleBox : 0));
     if (stma ? lane == 0 : true) {
       for (int st = 0; st < total_st && !a.test_fault; ++st) {
         const int s = st % L::stages;
@@ -279,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
               const uint32_t hi = (row < PU.n && g + 1 < PU.G) ? __ldg(src + 1) : 0u;
               v[j] = lo | (hi << 16);
             }
-            *reinterpret_cast<uint4*>(slot + FT::nb * kBox + (lane + 32 * i) * 16) = make_uint4(v[0], v[1], v[2], v[3]);
+            *reinterpret_cast<uint4*>(slot + FT::nb * FT::box + (lane + 32 * i) * 16) = make_uint4(v[0], v[1], v[2], v[3]);
           }
           if (lane != 0) lbdev::mbar_arrive(&full[s]);
         }
@@ -287,8 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
           lbdev::mbar_arrive_expect_tx(&full[s], bytes);
 #pragma unroll
           for (int b = 0; b < FT::nb; ++b)
-            lbdev::tma_load_2d(slot + b * kBox, &PU.tm_codes, (g0 + b * (GS / FT::nb)) * FT::gbytes, row0, &full[s]);
-          if (stma) lbdev::tma_load_2d(slot + FT::nb * kBox, &PU.tm_scales, g0, row0, &full[s]);
+            lbdev::tma_load_2d(slot + b * FT::box, &PU.tm_codes, (g0 + b * (GS / FT::nb)) * FT::gbytes, row0, &full[s]);
+          if (stma) lbdev::tma_load_2d(slot + FT::nb * FT::box, &PU.tm_scales, g0, row0, &full[s]);
           LB_TRACE(st == 0, 1);
           LB_TRACE(st == total_st - 1, 2);
         }
@@ -297,7 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     __syncwarp();
     griddep_launch();
   } else if constexpr (L::LU) {
-    // ======================= consumers, 1-bit lookup-table form (batch 1).  Per chunk of four
+    // ======================= consumers, lookup-table form (batch 1; 1-bit, and ternary five per
+    // byte, whose tables are described at the build below).  1-bit: per chunk of four
     // activations the table holds the 16 signed sums sum_i (b_i ? +x_i : -x_i) (FP32, in the
     // chunk's 64 bytes), so a code nibble b_0..b_3 costs one lookup and one add: thread = weight row,
     // warp = 32 rows x 2 of a stage's 8 groups; four warps share rows and add up at the row block's
@@ -313,9 +321,43 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     // 16-byte stores are contiguous (no bank conflicts).  The entries are FP32 sums of the exact
     // activations, built in one pass; bfloat16 columns whose largest magnitude is 2^100 or more
     // (where sums of four could overflow) are built again scaled down by a power of two.
-    const int items = L::pad(ng > 0 ? ng : 0) * 32 * 4;
+    const int items = L::pad(ng > 0 ? ng : 0) * (FMT == 3 ? 104 : 128);
+    auto bf_exp = [](uint32_t u) { return u & 0x7f800000u; };     // a bfloat16 pattern's exponent field
+    auto act = [&](int i, float scale) -> float {                   // activation i of the CTA's chunk
+      const uint32_t u = static_cast<uint32_t>(xrow[i]);
+      return XBF ? __uint_as_float(u << 16) * scale : __half2float(__ushort_as_half(static_cast<unsigned short>(u)));
+    };
     auto build = [&](float scale) -> uint32_t {
       uint32_t mx = 0;
+      if constexpr (FMT == 3) {
+        // five per byte: byte j of a group holds digits d0..d4 (weights 5j .. 5j+4); slot j of the
+        // group's table holds A[d0 + 3 d1] = (d0 - 1) x_5j + (d1 - 1) x_5j+1 (9 floats) and then
+        // B[d2 + 3 d3 + 9 d4] = sum (d - 1) x over weights 5j+2 .. 5j+4 (27 floats); weights past
+        // 127 (byte 25) count as x = 0.  Item i = (group, j, part): part 0 writes A, part p > 0
+        // the nine B entries with d4 = p - 1, at floats 9 i .. 9 i + 8 (no bank conflicts).
+        for (int it = threadIdx.x; it < items; it += NW * 32) {
+          const int g = it / 104, rem = it - g * 104, j = rem >> 2, part = rem & 3;
+          const int k0 = 5 * j + (part == 0 ? 0 : 2);               // first weight of the part
+          float v[3] = {0.f, 0.f, 0.f};
+#pragma unroll
+          for (int q = 0; q < 3; ++q) {
+            const int kk = k0 + q;
+            if ((part != 0 || q < 2) && kk < 128 && g < ng) {
+              if (XBF) mx = max(mx, bf_exp(static_cast<uint32_t>(xrow[g * 128 + kk]) << 16));
+              v[q] = act(g * 128 + kk, scale);
+            }
+          }
+          float* dst = tab + 9 * it;
+          if (part == 0) {
+#pragma unroll
+            for (int e = 0; e < 9; ++e) dst[e] = (e % 3 - 1) * v[0] + (e / 3 - 1) * v[1];
+          } else {
+            const float c = (part - 2) * v[2];                       // (d4 - 1) x_5j+4
+#pragma unroll
+            for (int e = 0; e < 9; ++e) dst[e] = ((e % 3 - 1) * v[0] + (e / 3 - 1) * v[1]) + c;
+          }
+        }
+      } else {
 #pragma unroll 4
       for (int t = threadIdx.x; t < items; t += NW * 32) {
         const int c = t >> 2, h = t & 3;
@@ -336,6 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         const float lo4[4] = {-v[0] - v[1], v[0] - v[1], v[1] - v[0], v[0] + v[1]};   // bits 0, 1
         const float hi = ((h & 1) ? v[2] : -v[2]) + ((h & 2) ? v[3] : -v[3]);         // bits 2, 3 = h
         reinterpret_cast<float4*>(tab)[t] = make_float4(lo4[0] + hi, lo4[1] + hi, lo4[2] + hi, lo4[3] + hi);
+      }
       }
       return mx;
     };
@@ -361,9 +404,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     const int row_l = 32 * rq + lane;
     const uint32_t sm32 = lbdev::smem_u32(sm);
     const uint32_t tb = sm32 + static_cast<uint32_t>(L::xs(gpc));   // 256-byte aligned
-    const uint32_t code0 = static_cast<uint32_t>(row_l * 128 + (((2 * kq) ^ (row_l & 7)) << 4));
+    const uint32_t code0 = static_cast<uint32_t>(row_l * 128 + (((2 * kq) ^ (row_l & 7)) << 4));   // 1-bit
     const uint32_t code1 = static_cast<uint32_t>(row_l * 128 + (((2 * kq + 1) ^ (row_l & 7)) << 4));
-    const uint32_t sc_off = static_cast<uint32_t>(kBox + row_l * 16 + 4 * kq);
+    const uint32_t sc_off = static_cast<uint32_t>(FT::nb * FT::box + row_l * 16 + 4 * kq);
     float acc = 0.f;
     int s = 0, st = 0;
     uint32_t ph = 0;
@@ -374,16 +417,45 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         ok = __all_sync(0xffffffffu, ok);
         LB_TRACE(threadIdx.x == 0 && st < 16, 5 + st);
         uint4 w[2];
+        uint32_t c13[13];                                          // five per byte: my 52 code bytes
         uint32_t sc2 = 0;
         if (ok) {
-          w[0] = ldsv128(slot + code0);
-          w[1] = ldsv128(slot + code1);
+          if constexpr (FMT == 3) {
+            // the row's 208 bytes of the stage, my two groups at byte 52 kq (4-byte aligned)
+#pragma unroll
+            for (int i = 0; i < 13; ++i) c13[i] = ldsv32(slot + static_cast<uint32_t>(row_l * 208 + 52 * kq + 4 * i));
+          } else {
+            w[0] = ldsv128(slot + code0);
+            w[1] = ldsv128(slot + code1);
+          }
           sc2 = ldsv32(slot + sc_off);
         }
         __syncwarp();
         if (lane == 0) lbdev::mbar_arrive(&empty[s]);             // slot s released by this warp
         if (++s == L::stages) { s = 0; ph ^= 1u; }
-        if (ok && cstage * GS + 2 * kq < ng) {
+        if (FMT == 3 && ok && cstage * GS + 2 * kq < ng) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            // byte b = sum d_i 3^i: b mod 9 indexes A (two weights), b / 9 = (57 b) >> 9 (exact for
+            // b <= 242) indexes B (three weights) of the byte's table slot (144 bytes)
+            const uint32_t base = tb + static_cast<uint32_t>((cstage * GS + 2 * kq + h) * (26 * 36 * 4));
+            float p4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int j = 0; j < 26; ++j) {
+              const int kb = 26 * h + j;
+              const uint32_t b = __byte_perm(c13[kb >> 2], 0u, 0x4440u | static_cast<uint32_t>(kb & 3));
+              const uint32_t q = (b * 57u) >> 9;
+              const uint32_t r = b - 9u * q;
+              float ta, tbv;
+              asm("ld.shared.f32 %0, [%1];" : "=f"(ta) : "r"(base + static_cast<uint32_t>(j * 144) + 4u * r));
+              asm("ld.shared.f32 %0, [%1];" : "=f"(tbv) : "r"(base + static_cast<uint32_t>(j * 144 + 36) + 4u * q));
+              p4[j & 3] += ta + tbv;
+            }
+            const float sg = __half2float(__ushort_as_half(static_cast<unsigned short>(sc2 >> (16 * h))));
+            acc = fmaf(sg, (p4[0] + p4[1]) + (p4[2] + p4[3]), acc);
+          }
+        }
+        if (FMT == 1 && ok && cstage * GS + 2 * kq < ng) {
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             // the chunk of nibble j of word u is 8u + j of the group: low byte (j % 4) * 64 + 4 * idx,
@@ -598,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     const uint32_t sm32 = lbdev::smem_u32(sm);
     const uint32_t xs_lane = sm32 + static_cast<uint32_t>(L::xs(gpc)) + lane * 16 + tok;
     const uint32_t cn_q = sm32 + static_cast<uint32_t>(L::cneg) + 16 * q + tok;
-    const uint32_t sc_off = static_cast<uint32_t>(FT::nb * kBox + ia * 16 + half * 8);
+    const uint32_t sc_off = static_cast<uint32_t>(FT::nb * FT::box + ia * 16 + half * 8);
     const float mul = FMT == 1 ? 2.f : 1.f;
     const int c0col = 2 * q, c1col = 2 * q + 1;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -865,10 +937,12 @@ lb_status encode_maps(const lb_weight& W, CUtensorMap& tm_codes, CUtensorMap& tm
   {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k) * gbytes / 128, static_cast<cuuint64_t>(n)};
     const cuuint64_t strides[1] = {dims[0]};
-    const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(ROWS)};
+    // 2-bit / 1-bit: 128-byte boxes, 128-byte swizzle; five per byte: 8 groups = 208 bytes, no swizzle
+    const cuuint32_t box[2] = {FMT == 3 ? 8u * 26u : 128u, static_cast<cuuint32_t>(ROWS)};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(&tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(W.codes), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     FMT == 3 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return lb::fail(LB_ERR_CUDA, "lb_gemv: codes tensor map (CUresult %d)", static_cast<int>(r));
   }
@@ -1158,10 +1232,20 @@ EncodeTiledFn tensor_map_encoder() {
   return fn;
 }
 
+// Five per byte at batch 1 on the lookup-table consumer: needs TMA-able code rows (26 G bytes a
+// multiple of 16, i.e. G % 8 == 0) and a table that fits some K split.
+bool gemv_t5_lut_ok(const lb_weight& W, int batch) {
+  const int G = static_cast<int>(W.k / kGroup);
+  return batch == 1 && G % 8 == 0 &&
+         plan_split<3, 0>(G, static_cast<int>((W.n + ROWS - 1) / ROWS), sm_count()).S != 0;
+}
+
 lb_status launch_gemv(const lb_weight& W, const void* x, int xdt, int batch, void* y, cudaStream_t st) {
   const uint16_t* xs = static_cast<const uint16_t*>(x);
   uint16_t* ys = static_cast<uint16_t*>(y);
   const bool bf = xdt == LB_BF16;
+  if (W.fmt == LB_FMT_TERNARY5_G128)                               // callers checked gemv_t5_lut_ok
+    return bf ? launch_t<3, true, 0>(W, xs, batch, ys, st) : launch_t<3, false, 0>(W, xs, batch, ys, st);
   if (W.fmt == LB_FMT_1BIT_G128)
     return bf ? launch_b<1, true>(W, xs, batch, ys, st) : launch_b<1, false>(W, xs, batch, ys, st);
   return bf ? launch_b<2, true>(W, xs, batch, ys, st) : launch_b<2, false>(W, xs, batch, ys, st);
