@@ -283,7 +283,9 @@ GEMV_ROWS = (  # row name, workload, batch, grouping[, storage]
     ("gemv_c4b_b1", "c4b", 1, "layer"),
     ("gemv_c4b_b5", "c4b", 5, "layer"),
     ("gemv_c4t_b1_5launches", "c4t", 1, "separate"),
+    ("gemv_c2_b1_ternary5", "c2", 1, "layer", "ternary5"),
     ("gemv_c2_b1_ternary5_7launches", "c2", 1, "separate", "ternary5"),
+    ("gemv_c4t_b1_ternary5", "c4t", 1, "layer", "ternary5"),
     ("gemv_c4t_b1_ternary5_5launches", "c4t", 1, "separate", "ternary5"),
     ("gemv_c4t_b5_ternary5_5launches", "c4t", 5, "separate", "ternary5"),
 )

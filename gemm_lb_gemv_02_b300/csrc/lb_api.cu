@@ -237,8 +237,6 @@ lb_status lb_gemv_batched(const lb_gemv_problem* problems, int count, int xdt, i
     if (s != LB_OK) return s;
     if (pb.W.fmt != problems[0].W.fmt)
       return fail(LB_ERR_UNSUPPORTED, "problem %d: every problem of one call must have the same format", i);
-    if (pb.W.fmt == LB_FMT_TERNARY5_G128)
-      return fail(LB_ERR_UNSUPPORTED, "lb_gemv_batched takes the 1-bit and 2-bit ternary formats");
     if (!pb.x || !pb.y) return fail(LB_ERR_NULL, "problem %d: x and y must be non-NULL", i);
     if (!lb::aligned16(pb.x) || !lb::aligned16(pb.y)) return fail(LB_ERR_ALIGN, "problem %d: x and y must be 16-byte aligned", i);
   }

@@ -321,40 +321,58 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     // 16-byte stores are contiguous (no bank conflicts).  The entries are FP32 sums of the exact
     // activations, built in one pass; bfloat16 columns whose largest magnitude is 2^100 or more
     // (where sums of four could overflow) are built again scaled down by a power of two.
-    const int items = L::pad(ng > 0 ? ng : 0) * (FMT == 3 ? 104 : 128);
+    const int items = L::pad(ng > 0 ? ng : 0) * 128;
     auto bf_exp = [](uint32_t u) { return u & 0x7f800000u; };     // a bfloat16 pattern's exponent field
-    auto act = [&](int i, float scale) -> float {                   // activation i of the CTA's chunk
-      const uint32_t u = static_cast<uint32_t>(xrow[i]);
-      return XBF ? __uint_as_float(u << 16) * scale : __half2float(__ushort_as_half(static_cast<unsigned short>(u)));
-    };
     auto build = [&](float scale) -> uint32_t {
       uint32_t mx = 0;
       if constexpr (FMT == 3) {
         // five per byte: byte j of a group holds digits d0..d4 (weights 5j .. 5j+4); slot j of the
-        // group's table holds A[d0 + 3 d1] = (d0 - 1) x_5j + (d1 - 1) x_5j+1 (9 floats) and then
-        // B[d2 + 3 d3 + 9 d4] = sum (d - 1) x over weights 5j+2 .. 5j+4 (27 floats); weights past
-        // 127 (byte 25) count as x = 0.  Item i = (group, j, part): part 0 writes A, part p > 0
-        // the nine B entries with d4 = p - 1, at floats 9 i .. 9 i + 8 (no bank conflicts).
-        for (int it = threadIdx.x; it < items; it += NW * 32) {
-          const int g = it / 104, rem = it - g * 104, j = rem >> 2, part = rem & 3;
-          const int k0 = 5 * j + (part == 0 ? 0 : 2);               // first weight of the part
-          float v[3] = {0.f, 0.f, 0.f};
+        // group's table (144 bytes, at (26 g + j) * 144) holds A[d0 + 3 d1] = (d0 - 1) x_5j +
+        // (d1 - 1) x_5j+1 (9 floats) and then B[d2 + 3 d3 + 9 d4] = sum (d - 1) x over weights
+        // 5j+2 .. 5j+4 (27 floats); weights past 127 (byte 25) count as x = 0.  A thread builds
+        // whole slots: it loads the slot's five activations (the loads of all its slots issued
+        // together), forms the 36 sums in registers and writes them as nine 16-byte stores
+        // (slots 144 bytes apart: no bank conflicts).
+        const int slots = L::pad(ng > 0 ? ng : 0) * 26;
+        constexpr int kS = 3;                                      // 3 x 512 >= 26 x 40 slots
+        for (int t0 = threadIdx.x; t0 < slots; t0 += kS * NW * 32) {
+          uint32_t raw[kS][5];
 #pragma unroll
-          for (int q = 0; q < 3; ++q) {
-            const int kk = k0 + q;
-            if ((part != 0 || q < 2) && kk < 128 && g < ng) {
-              if (XBF) mx = max(mx, bf_exp(static_cast<uint32_t>(xrow[g * 128 + kk]) << 16));
-              v[q] = act(g * 128 + kk, scale);
+          for (int u = 0; u < kS; ++u) {
+            const int it = t0 + u * NW * 32;
+            const int g = it / 26, j = it - g * 26;
+#pragma unroll
+            for (int q = 0; q < 5; ++q) {
+              const int kk = 5 * j + q;
+              raw[u][q] = (it < slots && kk < 128 && g < ng) ? static_cast<uint32_t>(__ldg(xrow + g * 128 + kk)) : 0u;
             }
           }
-          float* dst = tab + 9 * it;
-          if (part == 0) {
 #pragma unroll
-            for (int e = 0; e < 9; ++e) dst[e] = (e % 3 - 1) * v[0] + (e / 3 - 1) * v[1];
-          } else {
-            const float c = (part - 2) * v[2];                       // (d4 - 1) x_5j+4
+          for (int u = 0; u < kS; ++u) {
+            const int it = t0 + u * NW * 32;
+            if (it >= slots) break;
+            float v[5];
 #pragma unroll
-            for (int e = 0; e < 9; ++e) dst[e] = ((e % 3 - 1) * v[0] + (e / 3 - 1) * v[1]) + c;
+            for (int q = 0; q < 5; ++q) {
+              if (XBF) {
+                mx = max(mx, bf_exp(raw[u][q] << 16));
+                v[q] = __uint_as_float(raw[u][q] << 16) * scale;
+              } else {
+                v[q] = __half2float(__ushort_as_half(static_cast<unsigned short>(raw[u][q])));
+              }
+            }
+            float e36[36];
+#pragma unroll
+            for (int e = 0; e < 9; ++e) {
+              e36[e] = (e % 3 - 1) * v[0] + (e / 3 - 1) * v[1];
+              const float p23 = (e % 3 - 1) * v[2] + (e / 3 - 1) * v[3];
+#pragma unroll
+              for (int d4 = 0; d4 < 3; ++d4) e36[9 + e + 9 * d4] = p23 + (d4 - 1) * v[4];
+            }
+            float4* dst = reinterpret_cast<float4*>(tab + 36 * it);
+#pragma unroll
+            for (int c = 0; c < 9; ++c)
+              dst[c] = make_float4(e36[4 * c], e36[4 * c + 1], e36[4 * c + 2], e36[4 * c + 3]);
           }
         }
       } else {
@@ -421,9 +439,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         uint32_t sc2 = 0;
         if (ok) {
           if constexpr (FMT == 3) {
-            // the row's 208 bytes of the stage, my two groups at byte 52 kq (4-byte aligned)
+            // the row's 208 bytes of the stage (13 x 16 bytes: a warp's 16-byte loads hit every
+            // bank once per quarter), my two groups at byte 52 kq: four 16-byte loads from the
+            // 16-byte boundary below, then a shift by 52 kq mod 16 = 4 kq bytes (warp-uniform)
+            uint32_t w16[16];
 #pragma unroll
-            for (int i = 0; i < 13; ++i) c13[i] = ldsv32(slot + static_cast<uint32_t>(row_l * 208 + 52 * kq + 4 * i));
+            for (int c = 0; c < 4; ++c) {
+              const uint4 v = ldsv128(slot + static_cast<uint32_t>(row_l * 208 + ((52 * kq) & ~15) + 16 * c));
+              w16[4 * c] = v.x; w16[4 * c + 1] = v.y; w16[4 * c + 2] = v.z; w16[4 * c + 3] = v.w;
+            }
+            uint32_t t15[15];
+#pragma unroll
+            for (int i = 0; i < 15; ++i) t15[i] = (kq & 1) ? w16[i + 1] : w16[i];
+#pragma unroll
+            for (int i = 0; i < 13; ++i) c13[i] = (kq & 2) ? t15[i + 2] : t15[i];
           } else {
             w[0] = ldsv128(slot + code0);
             w[1] = ldsv128(slot + code1);
@@ -849,29 +878,32 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   }
 
   if (a.S > 1) {
-    // one row block per cluster: every rank with a K chunk pushed its partials to the rows'
-    // owners; one cluster barrier (every thread of every CTA, producer warp included) and each
-    // owner sums its rows locally, in rank order.  No CTA touches another's shared memory after it.
+    // one or two row blocks per cluster (or one fused pair): every rank with a K chunk pushed its
+    // partials of each unit to the rows' owners; one cluster barrier (every thread of every CTA,
+    // producer warp included) and each owner sums its rows locally, in rank order.  No CTA touches
+    // another's shared memory after it.
     cluster_sync();
     if (warp < NW) {
-      const int rb = rb0;
       const int per = (ROWS + a.S - 1) / a.S;
       const int lo = static_cast<int>(rank) * per, hi = min(ROWS, lo + per);
       const int nrank = min(a.S, (P.G + gpc - 1) / gpc);           // ranks that had groups
       const float* xchg = reinterpret_cast<const float*>(sm + L::xchg);
-      for (int e = threadIdx.x; e < (hi - lo) * a.batch; e += NW * 32) {
-        const int lrow = lo + e / a.batch, col = e % a.batch;
-        const int row = rb * ROWS + lrow;
-        float v = 0.f;
-        for (int p = 0; p < nrank; ++p) v += xchg[(p * per + lrow - lo) * 8 + col];
-        if (a.fuse) {                                              // v is the gate; the up partials follow
-          float u = 0.f;
-          for (int p = 0; p < nrank; ++p) u += xchg[((a.S + p) * per + lrow - lo) * 8 + col];
-          v = silu(v) * u;
+      for (int u0 = 0; u0 < (a.fuse ? 1 : my_rbs); ++u0) {
+        const int rb = a.fuse ? rb0 : unit_rb(u0);
+        for (int e = threadIdx.x; e < (hi - lo) * a.batch; e += NW * 32) {
+          const int lrow = lo + e / a.batch, col = e % a.batch;
+          const int row = rb * ROWS + lrow;
+          float v = 0.f;
+          for (int p = 0; p < nrank; ++p) v += xchg[((u0 * a.S + p) * per + lrow - lo) * 8 + col];
+          if (a.fuse) {                                            // v is the gate; the up partials follow
+            float u = 0.f;
+            for (int p = 0; p < nrank; ++p) u += xchg[((a.S + p) * per + lrow - lo) * 8 + col];
+            v = silu(v) * u;
+          }
+          if (row < P.n)
+            P.y[static_cast<int64_t>(col) * P.n + row] =
+                XBF ? __bfloat16_as_ushort(__float2bfloat16_rn(v)) : __half_as_ushort(__float2half_rn(v));
         }
-        if (row < P.n)
-          P.y[static_cast<int64_t>(col) * P.n + row] =
-              XBF ? __bfloat16_as_ushort(__float2bfloat16_rn(v)) : __half_as_ushort(__float2half_rn(v));
       }
     }
   }
@@ -884,15 +916,17 @@ int pad_batch(int b) { return b <= 1 ? 1 : b <= 2 ? 2 : b <= 4 ? 4 : 8; }
 
 // Split of K across a cluster (S CTAs, chunk of gpc groups) from a simple time model: every CTA
 // pays a fixed cost (launch ramp, x prologue, first TMA latency; more with a cluster reduction),
-// then streams its row blocks x groups at the per-SM share of HBM bandwidth.
+// then streams its row blocks x groups at the per-SM share of HBM bandwidth.  A cluster takes one
+// row block or two (rpc; the exchange buffer holds two units' partials), which matters when S x
+// the row blocks would not fit on the SMs in one wave.
 struct Plan {
-  int S, gpc;
+  int S, gpc, rpc;
 };
 template <int FMT, int BP>
 Plan plan_split(int G, int row_blocks, int sms) {
   using L = Layout<FMT, BP>;
   const double t_group = (L::LU ? 0.5 : 1.0) * 16384.0 * (FmtTraits<FMT>::gbytes + 2) / 128.0 / 40.0;   // ns per 128x128 tile
-  Plan best{0, 0};
+  Plan best{0, 0, 1};
   double best_t = 1e30;
   for (int s_try = 1; s_try <= kMaxCluster; ++s_try) {
     const int per = (G + s_try - 1) / s_try;
@@ -900,16 +934,19 @@ Plan plan_split(int G, int row_blocks, int sms) {
     const int s_eff = (G + g_try - 1) / g_try;
     if (s_eff != s_try) continue;
     if (L::total(g_try) > kSmemMax) continue;
-    double t;
     if (s_eff == 1) {
       const int per_cta = (row_blocks + sms - 1) / sms;
-      t = 2500.0 + per_cta * g_try * t_group;
-    } else {
-      const int clusters = max(1, sms / s_eff);
-      const int waves = (row_blocks + clusters - 1) / clusters;
-      t = waves * (3000.0 + g_try * t_group);
+      const double t = 2500.0 + per_cta * g_try * t_group;
+      if (t < best_t * 0.999) { best_t = t; best = Plan{1, g_try, 1}; }
+      continue;
     }
-    if (t < best_t * 0.999) { best_t = t; best = Plan{s_eff, g_try}; }
+    const int clusters = max(1, sms / s_eff);
+    for (int r = 1; r <= 2; ++r) {
+      const int need = (row_blocks + r - 1) / r;
+      const int waves = (need + clusters - 1) / clusters;
+      const double t = waves * (3000.0 + r * g_try * t_group);
+      if (t < best_t * 0.999) { best_t = t; best = Plan{s_eff, g_try, r}; }
+    }
   }
   return best;
 }
@@ -1054,7 +1091,8 @@ lb_status launch_t(const lb_weight& W, const uint16_t* x, int batch, uint16_t* y
   args.count = 1;
   args.batch = batch;
   args.S = plan.S;
-  return launch_args<FMT, XBF, BP>(args, plan.S, plan.S > 1 ? row_blocks : min(row_blocks, sms),
+  return launch_args<FMT, XBF, BP>(args, plan.S,
+                                   plan.S > 1 ? (row_blocks + plan.rpc - 1) / plan.rpc : min(row_blocks, sms),
                                    L::total(plan.gpc), st);
 }
 
@@ -1264,6 +1302,18 @@ lb_status launch_gemv_swiglu(const lb_weight& Wg, const lb_weight& Wu, const voi
 lb_status launch_gemv_batched(const lb_gemv_problem* probs, int count, int xdt, int batch, cudaStream_t st) {
   if (count > kMaxProblems) return fail(LB_ERR_SHAPE, "lb_gemv_batched: count %d > %d", count, kMaxProblems);
   const bool bf = xdt == LB_BF16;
+  if (probs[0].W.fmt == LB_FMT_TERNARY5_G128) {
+    // five per byte: one lookup-table launch at batch 1 when every problem's tables fit,
+    // otherwise one CUDA-core launch per problem
+    bool lut = true;
+    for (int i = 0; i < count; ++i) lut = lut && gemv_t5_lut_ok(probs[i].W, batch);
+    if (lut) return bf ? launch_many<3, true, 0>(probs, count, batch, st) : launch_many<3, false, 0>(probs, count, batch, st);
+    for (int i = 0; i < count; ++i) {
+      const lb_status s = launch_gemv_t5(probs[i].W, probs[i].x, xdt, batch, probs[i].y, st);
+      if (s != LB_OK) return s;
+    }
+    return LB_OK;
+  }
   if (probs[0].W.fmt == LB_FMT_1BIT_G128)
     return bf ? launch_mb<1, true>(probs, count, batch, st) : launch_mb<1, false>(probs, count, batch, st);
   return bf ? launch_mb<2, true>(probs, count, batch, st) : launch_mb<2, false>(probs, count, batch, st);

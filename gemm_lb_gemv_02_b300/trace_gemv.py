@@ -99,6 +99,8 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--xdtype", choices=["bf16", "f16"], default=None,
                     help="activation type (default: the workload's own)")
+    ap.add_argument("--ternary5", action="store_true",
+                    help="store a ternary workload's codes five per byte")
     a = ap.parse_args()
 
     from gemm_lb_gemv_02_b300 import build
@@ -116,9 +118,13 @@ def main() -> None:
     packed = []
     for i in range(len(wl.matrices)):
         inp = synth.matrix_inputs(wl, i)
-        packed.append(tensors.pack_1bit(inp["w"].cuda()) if wl.fmt == "1bit"
-                      else tensors.pack_ternary(inp["t"].cuda(), inp["s"].cuda()))
-    layers = LAYERS.get(a.workload, [[n] for n in names])
+        if wl.fmt == "1bit":
+            packed.append(tensors.pack_1bit(inp["w"].cuda()))
+        else:
+            pack = tensors.pack_ternary5 if a.ternary5 else tensors.pack_ternary
+            packed.append(pack(inp["t"].cuda(), inp["s"].cuda()))
+    # the five-per-byte format has no multi-problem launch: one launch per matrix
+    layers = [[n] for n in names] if a.ternary5 else LAYERS.get(a.workload, [[n] for n in names])
     groups = [[names.index(n) for n in g] for g in layers]
     xs = {g[0]: synth.workload_activations(wl, g[0], a.batch).cuda() for g in groups}
     if a.xdtype:
@@ -144,7 +150,8 @@ def main() -> None:
     clock_ghz = torch.cuda.get_device_properties(0).clock_rate / 1e6 if hasattr(
         torch.cuda.get_device_properties(0), "clock_rate") else 1.92
     print(f"## GEMV phase trace: {a.workload}, launch {a.launch} "
-          f"({'+'.join(layers[a.launch])}), batch {a.batch}, x {next(iter(xs.values())).dtype}\n")
+          f"({'+'.join(layers[a.launch])}), batch {a.batch}, x {next(iter(xs.values())).dtype}"
+          f"{', five per byte' if a.ternary5 else ''}\n")
     print(summarize(buf, clock_ghz))
 
 

@@ -39,8 +39,8 @@
  *     validation result, so their LB_OK means "done and valid".
  *   - Thread safety: every call may be made from any host thread; pack calls serialise on an
  *     internal mutex (they share one device-side validation word per device).
- *   - Launch order: lb_gemv (1-bit and 2-bit ternary weights), lb_gemv_batched and lb_gemv_swiglu
- *     are launched with programmatic dependent launch.  Such a launch may start while the kernel
+ *   - Launch order: lb_gemv, lb_gemv_batched and lb_gemv_swiglu are launched with programmatic
+ *     dependent launch (the five-per-byte format only on its batch-1 lookup-table path).  Such a launch may start while the kernel
  *     enqueued just before it on `stream` is still running; it reads x and writes y only after
  *     that kernel has completed, but it starts streaming the packed weights (codes and scales)
  *     before.  The weights must therefore not be written by the kernel that immediately precedes
@@ -48,7 +48,7 @@
  *     synchronisation.  The pack calls synchronise, so packing and then multiplying is safe.
  *     Activations and outputs carry no such restriction (x may come from the preceding kernel, y
  *     may be read by the next one).  lb_gemm, lb_gemm_noalloc, lb_embed and the five-per-byte
- *     GEMV wait for the preceding kernel before reading anything.
+ *     GEMV's CUDA-core path wait for the preceding kernel before reading anything.
  */
 #ifndef LB_H_
 #define LB_H_
@@ -154,8 +154,11 @@ lb_status lb_pack_ternary5(const int8_t* t, const uint16_t* s_in, int64_t n, int
  *     y[b][n] = sum_g s[n][g] * sum_{i<128} t[n][128g+i] * x[b][128g+i],   0 <= b < batch,
  * with FP32 accumulation, rounded once to the dtype of x (round to nearest even).
  *
- * W     : packed matrix (n x k), any format; the five-per-byte ternary format runs a CUDA-core
- *         kernel that decodes a code byte through a 243-entry table (no K limit).
+ * W     : packed matrix (n x k), any format.  The five-per-byte ternary format at batch 1 with
+ *         k a multiple of 1024 runs the pipelined kernel of the other formats, adding per code
+ *         byte two entries of shared-memory tables of signed activation sums (k <= 40960, where
+ *         the tables of a K chunk fit one CTA of an 8-CTA cluster); otherwise it runs a CUDA-core kernel
+ *         that decodes a code byte through a 243-entry table (no K limit).
  * x     : device [batch][k] of `xdt`, 16-byte aligned.     y : device [batch][n] of `xdt`.
  * batch : 1 .. 8.
  * Asynchronous on `stream`.  Errors (no launch): LB_ERR_NULL, LB_ERR_SHAPE, LB_ERR_ALIGN,
@@ -182,6 +185,8 @@ typedef struct lb_gemv_problem {
  * lb_gemv computes for it; problems may differ in n, k, x and y (x buffers may be shared).
  *
  * problems : host array of `count` problems, 1 <= count <= LB_GEMV_BATCH_MAX, all of the same format.
+ *            Five per byte: one launch when lb_gemv would take the lookup-table path for every
+ *            problem, otherwise one CUDA-core launch per problem, in order.
  * xdt      : LB_F16 or LB_BF16 for every x and y;  batch : 1 .. 8 for every problem.
  * No y may overlap another problem's x or y.  Asynchronous on `stream`.  Errors (no launch):
  * LB_ERR_NULL, LB_ERR_SHAPE (count or batch out of range, a bad n / k), LB_ERR_ALIGN, LB_ERR_DTYPE,

@@ -108,7 +108,7 @@ def test_gemm_validation():
 
 
 def test_ternary5_entry_points():
-    """The five-per-byte format: sizes, packer validation, and the products that do not take it."""
+    """The five-per-byte format: sizes, packer validation, and the calls that do not take it."""
     assert lb.lb_packed_bytes(lb.LB_FMT_TERNARY5_G128, 3, 1024) == (3 * 8 * 26, 3 * 8 * 2)
     assert _status(lb.lb_pack_ternary5, A16, A16, 4, 100, A16, A16) == "LB_ERR_SHAPE"
     assert _status(lb.lb_pack_ternary5, None, A16, 4, 128, A16, A16) == "LB_ERR_NULL"
@@ -118,7 +118,9 @@ def test_ternary5_entry_points():
     assert _status(lb.lb_gemm, W5, A16, lb.LB_BF16, 5, A16, lb.LB_BF16, A16, need, 0) == "LB_ERR_UNSUPPORTED"
     assert _status(lb.lb_gemm_noalloc, W5, A16, lb.LB_BF16, 5, A16, lb.LB_BF16) == "LB_ERR_UNSUPPORTED"
     assert _status(lb.lb_embed, W5, A16, 3, A16, lb.LB_BF16, 0) == "LB_ERR_UNSUPPORTED"
-    assert _status(lb.lb_gemv_batched, [(W5, A16, A16)], lb.LB_F16, 1) == "LB_ERR_UNSUPPORTED"
+    # the grouped GEMV takes the format, but not mixed with another one in one call
+    W2 = lb.make_weight(lb.LB_FMT_TERNARY_G128, 256, 256, A16, A16)
+    assert _status(lb.lb_gemv_batched, [(W5, A16, A16), (W2, A16, A16)], lb.LB_F16, 1) == "LB_ERR_UNSUPPORTED"
     assert _status(lb.lb_gemv_swiglu, W5, W5, A16, lb.LB_F16, 1, A16, 0) == "LB_ERR_UNSUPPORTED"
     assert _status(lb.lb_gemv, W5, A16, lb.LB_F16, 9, A16, 0) == "LB_ERR_SHAPE"
 

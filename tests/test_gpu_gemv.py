@@ -201,3 +201,32 @@ def test_gemv_at_k_limit(fmt, batch, k):
     y = _run_guarded(pw, x)
     y_ref, a = oracle_products(fmt, codes, scales, k, x.cpu())
     check_products(y, y_ref, a, f"{fmt} k-limit batch={batch} k={k}")
+
+
+@pytest.mark.parametrize("fmt", ["1bit", "ternary"])
+@pytest.mark.parametrize("batch", [1, 8])
+def test_gemv_two_row_blocks_per_cluster(fmt, batch):
+    """9600 x 8192 splits K over 3-CTA clusters, and 75 row blocks x 3 CTAs do not fit the SMs in
+    one wave, so each cluster takes two row blocks (the second one grid-height row blocks after the
+    first) and reduces both through one exchange.  Sampled rows cover the first and last rows of
+    every row block."""
+    n, k = 9600, 8192
+    if fmt == "1bit":
+        inp = {"w": synth.weights_fp32(n, k, 0.05, seed=51)}
+        pw = tensors.pack_1bit(inp["w"].cuda())
+    else:
+        inp = {"t": synth.ternary_codes(n, k, seed=51), "s": synth.ternary_scales_bits(n, k, 0.02, seed=52)}
+        pw = tensors.pack_ternary(inp["t"].cuda(), inp["s"].cuda())
+    x = synth.activations(batch, k, "bf16", seed=53).cuda()
+    y = _run_guarded(pw, x)
+    rb = np.arange(0, n, 128)
+    rng = np.random.default_rng(54)
+    rows = np.unique(np.concatenate([rb, rb + 127, rng.integers(0, n, 1500)]))
+    sub = {key: v.numpy()[rows] for key, v in inp.items()}
+    if fmt == "1bit":
+        codes, scales = orc.pack_1bit(sub["w"])
+    else:
+        codes, scales = orc.pack_ternary(sub["t"], sub["s"].view(np.uint16))
+    y_ref, a = oracle_products(fmt, codes, scales, k, x.cpu())
+    check_products(y, y_ref, a, f"{fmt} {n}x{k} batch={batch}", cols=rows)
+

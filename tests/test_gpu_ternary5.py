@@ -94,3 +94,47 @@ def test_gemv_ternary5_integer_exact():
     torch.cuda.synchronize()
     y_ref, _ = orc.matvec(orc.FMT_TERNARY5, codes, scales, k, orc.f16_bits_to_f64(u16(x)))
     assert np.array_equal(orc.f16_bits_to_f64(u16(y)), y_ref)
+
+
+@pytest.mark.parametrize("name", ["gate", "down"])
+def test_gemv_ternary5_c4t_sampled_rows(name):
+    """The 27B-class gate (17408 x 5120) and down (5120 x 17408) matrices in five-per-byte storage
+    at batch 1 (lookup-table path; down splits K over 6-CTA clusters that take two row blocks
+    each), sampled rows including the first and last of every row block."""
+    wl = synth.WORKLOADS["c4t"]
+    gi = next(i for i, m in enumerate(wl.matrices) if m.name == name)
+    inp = synth.matrix_inputs(wl, gi)
+    pw = tensors.pack_ternary5(inp["t"].cuda(), inp["s"].cuda())
+    n, k = wl.matrices[gi].n, wl.matrices[gi].k
+    x = synth.workload_activations(wl, gi, 1).cuda()
+    y = tensors.gemv(pw, x)
+    torch.cuda.synchronize()
+    rb = np.arange(0, n, 128)
+    rng = np.random.default_rng(16)
+    rows = np.unique(np.concatenate([rb, rb + 127, rng.integers(0, n, 1000)]))
+    codes, scales = orc.pack_ternary5(inp["t"].numpy()[rows], inp["s"].numpy().view(np.uint16)[rows])
+    y_ref, a = orc.matvec(orc.FMT_TERNARY5, codes, scales, k, orc.decode_activation_bits(u16(x), "bf16"))
+    check_products(y, y_ref, a, f"c4t {name} ternary5", cols=rows)
+
+
+@pytest.mark.parametrize("batch", [1, 3])
+def test_gemv_ternary5_batched(batch):
+    """Grouped five-per-byte GEMVs: at batch 1 one lookup-table launch (problems sharing x and K run
+    on persistent CTAs with one table build; the others one CTA per row block), at batch 3 one
+    CUDA-core launch per problem.  Mixed n and k, a shared x."""
+    specs = [(1000, 4096, 0), (700, 4096, 0), (300, 2048, 1)]
+    xs = [synth.activations(batch, 4096, "bf16", seed=60).cuda(), synth.activations(batch, 2048, "bf16", seed=61).cuda()]
+    pws, refs = [], []
+    for i, (n, k, xi) in enumerate(specs):
+        t, s = _inputs(n, k, seed=62 + i)
+        pws.append(tensors.pack_ternary5(t.cuda(), s.cuda()))
+        refs.append(orc.pack_ternary5(t.numpy(), s.numpy().view(np.uint16)))
+    for group in ([0, 1], [0, 1, 2]):
+        ys = tensors.gemv_batched([(pws[i], xs[specs[i][2]]) for i in group])
+        torch.cuda.synchronize()
+        for i, y in zip(group, ys):
+            n, k, xi = specs[i]
+            xv = orc.decode_activation_bits(u16(xs[xi]), "bf16")
+            y_ref, a = orc.matvec(orc.FMT_TERNARY5, refs[i][0], refs[i][1], k, xv)
+            check_products(y, y_ref, a, f"ternary5 batched {group} problem {i} batch={batch}")
+
