@@ -123,8 +123,7 @@ def main() -> None:
         else:
             pack = tensors.pack_ternary5 if a.ternary5 else tensors.pack_ternary
             packed.append(pack(inp["t"].cuda(), inp["s"].cuda()))
-    # the five-per-byte format has no multi-problem launch: one launch per matrix
-    layers = [[n] for n in names] if a.ternary5 else LAYERS.get(a.workload, [[n] for n in names])
+    layers = LAYERS.get(a.workload, [[n] for n in names])
     groups = [[names.index(n) for n in g] for g in layers]
     xs = {g[0]: synth.workload_activations(wl, g[0], a.batch).cuda() for g in groups}
     if a.xdtype:
