@@ -97,3 +97,40 @@ def test_pack_full_size_lm_head_sampled():
     rows = np.unique(np.concatenate([[0, 1, n - 2, n - 1], rng.integers(0, n, 2000)]))
     rc, rs = orc.pack_1bit(w.numpy()[rows])
     assert np.array_equal(codes[rows], rc) and np.array_equal(scales[rows], rs)
+
+
+def _config_matrices():
+    out = []
+    for key in ("c1", "c2", "c4t", "c4b", "c5"):
+        wl = synth.WORKLOADS[key]
+        for i, m in enumerate(wl.matrices):
+            out.append((key, i, m.name))
+    return out
+
+
+@pytest.mark.parametrize("key,index,name", _config_matrices())
+def test_pack_every_config_matrix(key, index, name):
+    """Every matrix of every configuration at its own size, packed on the GPU with the library's
+    packers and compared bit-exactly with the oracle's packing: whole matrices up to 4096 rows,
+    otherwise the first, last and 1500 random rows.  Ternary matrices are also checked five per
+    byte."""
+    wl = synth.WORKLOADS[key]
+    inp = synth.matrix_inputs(wl, index)
+    n, k = wl.matrices[index].n, wl.matrices[index].k
+    rng = np.random.default_rng(index + 7)
+    rows = np.arange(n) if n <= 4096 else np.unique(np.concatenate([[0, 1, n - 2, n - 1], rng.integers(0, n, 1500)]))
+    if wl.fmt == "1bit":
+        codes, scales = _pack1(inp["w"])
+        rc, rs = orc.pack_1bit(inp["w"].numpy()[rows])
+        assert np.array_equal(codes[rows], rc) and np.array_equal(scales[rows], rs), f"{key}/{name} 1-bit"
+        return
+    t, s = inp["t"], inp["s"]
+    packers = [(tensors.pack_ternary, orc.pack_ternary, 32), (tensors.pack_ternary5, orc.pack_ternary5, 26)]
+    for dev_pack, ora_pack, gbytes in packers:
+        pw = dev_pack(t.cuda(), s.cuda())
+        torch.cuda.synchronize()
+        codes = u8(pw.codes).reshape(n, (k // 128) * gbytes)
+        scales = u16(pw.scales).reshape(n, k // 128)
+        rc, rs = ora_pack(t.numpy()[rows], s.numpy().view(np.uint16)[rows])
+        assert np.array_equal(codes[rows], rc) and np.array_equal(scales[rows], rs), f"{key}/{name} {gbytes} B/group"
+        del pw
