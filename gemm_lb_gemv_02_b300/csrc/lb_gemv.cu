@@ -914,9 +914,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 // ----------------------------------------------------------------------------- host side
 int pad_batch(int b) { return b <= 1 ? 1 : b <= 2 ? 2 : b <= 4 ? 4 : 8; }
 
+// Weight of one 128-row x 128-column tile against the fixed costs in the split model below (ns):
+// the packed bytes at ~40 B/ns (halved for the 1-bit tables), except for the five-per-byte
+// tables, whose measured stage period (~3.0 kcyc per 8 groups on B300) is used instead.  (With
+// the measured periods for every path, 2048-wide 1-bit GEMVs and the one-launch c2 set chose K
+// splits that measured slower.)
+template <int FMT, bool LU>
+constexpr double group_ns() {
+  return (LU && FMT == 3) ? 195.0 : (LU ? 0.5 : 1.0) * 16384.0 * (FmtTraits<FMT>::gbytes + 2) / 128.0 / 40.0;
+}
+
 // Split of K across a cluster (S CTAs, chunk of gpc groups) from a simple time model: every CTA
 // pays a fixed cost (launch ramp, x prologue, first TMA latency; more with a cluster reduction),
-// then streams its row blocks x groups at the per-SM share of HBM bandwidth.  A cluster takes one
+// then runs its row blocks x groups at group_ns each.  A cluster takes one
 // row block or two (rpc; the exchange buffer holds two units' partials), which matters when S x
 // the row blocks would not fit on the SMs in one wave.
 struct Plan {
@@ -925,7 +935,7 @@ struct Plan {
 template <int FMT, int BP>
 Plan plan_split(int G, int row_blocks, int sms) {
   using L = Layout<FMT, BP>;
-  const double t_group = (L::LU ? 0.5 : 1.0) * 16384.0 * (FmtTraits<FMT>::gbytes + 2) / 128.0 / 40.0;   // ns per 128x128 tile
+  const double t_group = group_ns<FMT, L::LU>();
   Plan best{0, 0, 1};
   double best_t = 1e30;
   for (int s_try = 1; s_try <= kMaxCluster; ++s_try) {
@@ -1112,7 +1122,7 @@ lb_status launch_many(const lb_gemv_problem* probs, int count, int batch, cudaSt
       order[j - 1] = t;
     }
   const int sms = lb::sm_count();
-  const double t_group = (L::LU ? 0.5 : 1.0) * 16384.0 * (FmtTraits<FMT>::gbytes + 2) / 128.0 / 40.0;   // ns per 128x128 tile
+  const double t_group = group_ns<FMT, L::LU>();
   int units = 0, gmax = 0;
   for (int i = 0; i < count; ++i) {
     units += static_cast<int>((probs[i].W.n + ROWS - 1) / ROWS);
@@ -1171,7 +1181,7 @@ lb_status launch_pair(const lb_weight& Wg, const lb_weight& Wu, const uint16_t* 
                       cudaStream_t st) {
   using L = Layout<FMT, BP>;
   const int sms = lb::sm_count();
-  const double t_group = (L::LU ? 0.5 : 1.0) * 16384.0 * (FmtTraits<FMT>::gbytes + 2) / 128.0 / 40.0;   // ns per 128x128 tile
+  const double t_group = group_ns<FMT, L::LU>();
   const int G = static_cast<int>(Wg.k / lb::kGroup);
   const int units = static_cast<int>((Wg.n + ROWS - 1) / ROWS);
   auto chunk = [](int g, int S) { return S == 1 ? g : ((g + S - 1) / S + GS - 1) / GS * GS; };
