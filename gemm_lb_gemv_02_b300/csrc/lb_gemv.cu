@@ -95,13 +95,18 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void st_dsmem(uint32_t local_addr, uint32_t rank, float v) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+// v into the shared memory of cluster CTA `rank`, at the image of `local_addr` there; the store
+// counts its 4 bytes on that CTA's mbarrier at the image of `local_bar` (complete_tx), which makes
+// the value visible to the threads that wait on that barrier.
+__device__ __forceinline__ void st_async_f32(uint32_t local_addr, uint32_t local_bar, uint32_t rank, float v) {
+  uint32_t ra, rb;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local_addr), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(local_bar), "r"(rank));
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(ra),
+               "r"(__float_as_uint(v)), "r"(rb)
+               : "memory");
 }
 // Phase trace (compiled in only with -DLB_GEMV_TRACE, for timing studies): per CTA, event e holds
 // {%globaltimer, clock64} of the moment one fixed thread passed a point of the kernel.  Events:
@@ -168,7 +173,8 @@ struct Layout {
   static constexpr int stages = FmtTraits<FMT>::stages;
   static constexpr int slot = FmtTraits<FMT>::nb * FmtTraits<FMT>::box + kScaleBox;
   static constexpr int ring = stages * slot;                     // 1024-byte aligned base
-  static constexpr int bars = ring;                              // full[stages], empty[stages]
+  static constexpr int bars = ring;                              // full[stages], empty[stages], xbar at 15
+  static_assert(2 * stages <= 15, "stage barriers and the exchange barrier share 128 bytes");
   static constexpr int red = bars + 128;                         // 2 x ROWS x 8 floats
   static constexpr int colf = red + 2 * ROWS * 8 * 4;            // 8 column factors + 8 column maxima
   // K split across a cluster: rank p's partial of row r (unit u) lands in the row's owner at
@@ -192,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   uint8_t* sm = smem_raw + ((1024u - (lbdev::smem_u32(smem_raw) & 1023u)) & 1023u);   // 1024-aligned
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + L::bars);
   uint64_t* empty = full + L::stages;
+  uint64_t* xbar = full + 15;                                    // K split: this CTA's exchange has landed
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   LB_TRACE(threadIdx.x == 0, 0);
@@ -243,10 +250,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
       lbdev::mbar_init(&full[s], P.scales_tma ? 1 : 32);         // 32: the lanes store the scales
       lbdev::mbar_init(&empty[s], NW);
     }
+    lbdev::mbar_init(xbar, 1);
     lbdev::fence_mbar_init();
   }
   if (threadIdx.x < 8) reinterpret_cast<uint32_t*>(sm + L::colf)[8 + threadIdx.x] = 0u;   // column maxima
   __syncthreads();
+  // K split: every thread arrives on the cluster barrier now and the consumers wait on it before
+  // their first remote store, so that no CTA's exchange barrier is used before it is initialised
+  // (by then the barrier has long completed, so the wait costs nothing)
+  if (a.S > 1) cluster_arrive();
 
   if (warp == NW) {
     // ======================= producer: weights do not depend on earlier kernels, so no wait.
@@ -417,6 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     }
     consumer_sync();
     LB_TRACE(threadIdx.x == 0, 4);
+    if (a.S > 1) cluster_wait();                                   // every exchange barrier is initialised
 
     const int rq = warp & 3, kq = warp >> 2;                      // rows 32 rq .., groups 2 kq, 2 kq + 1
     const int row_l = 32 * rq + lane;
@@ -531,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
           const int per = (ROWS + a.S - 1) / a.S;
           const int o = row_l / per;
           const int slot_i = ((i_rb * a.S + static_cast<int>(rank)) * per + (row_l - o * per)) * 8;
-          st_dsmem(sm32 + static_cast<uint32_t>(L::xchg + slot_i * 4), static_cast<uint32_t>(o), v);
+          st_async_f32(sm32 + static_cast<uint32_t>(L::xchg + slot_i * 4), lbdev::smem_u32(xbar), static_cast<uint32_t>(o), v);
         }
       }
       acc = 0.f;
@@ -670,6 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
       reinterpret_cast<uint4*>(xs)[i] = make_uint4(0u, 0u, 0u, 0u);  // x of the padding groups: zero
     consumer_sync();
     LB_TRACE(threadIdx.x == 0, 4);
+    if (a.S > 1) cluster_wait();                                   // every exchange barrier is initialised
 
     uint32_t tok;                                      // orders the private-region loads after the barrier
     asm volatile("mov.u32 %0, 0;" : "=r"(tok)::"memory");
@@ -853,15 +867,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             put(row_b, c1col, o3);
           } else {
             // this CTA's partial, in output units, goes straight into the shared memory of the
-            // cluster CTA that owns the row (fire and forget; the cluster barrier after the loop
-            // makes it visible)
+            // cluster CTA that owns the row, counted on that CTA's exchange barrier
             const int per = (ROWS + a.S - 1) / a.S;
             const uint32_t xchg = sm32 + static_cast<uint32_t>(L::xchg);
+            const uint32_t xb = lbdev::smem_u32(xbar);
             auto push = [&](int lrow, int col, float v) {
               if (col < a.batch) {
                 const int o = lrow / per;
                 const int slot_i = ((i_rb * a.S + static_cast<int>(rank)) * per + (lrow - o * per)) * 8 + col;
-                st_dsmem(xchg + static_cast<uint32_t>(slot_i * 4), static_cast<uint32_t>(o), v);
+                st_async_f32(xchg + static_cast<uint32_t>(slot_i * 4), xb, static_cast<uint32_t>(o), v);
               }
             };
             push(ia, c0col, v0);
@@ -877,31 +891,42 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     LB_TRACE(threadIdx.x == 0, 29);
   }
 
-  if (a.S > 1) {
-    // one or two row blocks per cluster (or one fused pair): every rank with a K chunk pushed its
-    // partials of each unit to the rows' owners; one cluster barrier (every thread of every CTA,
-    // producer warp included) and each owner sums its rows locally, in rank order.  No CTA touches
-    // another's shared memory after it.
-    cluster_sync();
-    if (warp < NW) {
-      const int per = (ROWS + a.S - 1) / a.S;
-      const int lo = static_cast<int>(rank) * per, hi = min(ROWS, lo + per);
-      const int nrank = min(a.S, (P.G + gpc - 1) / gpc);           // ranks that had groups
+  if (a.S > 1 && warp < NW) {
+    // one or two row blocks per cluster (or one fused pair): every rank pushed its partials of
+    // each unit to the rows' owners with remote stores that count their bytes on the owner's
+    // exchange barrier (every rank pushes every row it holds, also a rank without groups); each
+    // owner expects S x units x its rows x batch x 4 bytes, waits, and sums its rows locally, in
+    // rank order.  A CTA leaves only after its own exchange has landed, and no CTA stores into
+    // another after that CTA's exchange is complete.  The kernel parameters the owners need are
+    // read into registers before the wait.
+    int S_r = a.S, batch_r = a.batch, fuse_r = a.fuse, n_r = P.n, nrank = min(a.S, (P.G + gpc - 1) / gpc);
+    uint16_t* y_r = P.y;
+    int rbs_r[2] = {a.fuse ? rb0 : unit_rb(0), (!a.fuse && my_rbs > 1) ? unit_rb(1) : 0};
+    asm volatile("" : "+r"(S_r), "+r"(batch_r), "+r"(fuse_r), "+r"(n_r), "+r"(nrank), "+l"(y_r), "+r"(rbs_r[0]),
+                 "+r"(rbs_r[1]));
+    const int per = (ROWS + S_r - 1) / S_r;
+    const int lo = static_cast<int>(rank) * per, hi = min(ROWS, lo + per);
+    if (threadIdx.x == 0)
+      lbdev::mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(S_r * (fuse_r ? 2 : my_rbs) * (hi - lo) * batch_r * 4));
+    // twice the pipeline's limit: a rank that gave up on its own stages still pushes (zeros) within
+    // one limit of its start, so an owner never leaves while a late push is still to come
+    if (!lbdev::mbar_wait(xbar, 0, 2 * a.wait_ns)) ok = false;
+    if (ok) {
       const float* xchg = reinterpret_cast<const float*>(sm + L::xchg);
-      for (int u0 = 0; u0 < (a.fuse ? 1 : my_rbs); ++u0) {
-        const int rb = a.fuse ? rb0 : unit_rb(u0);
-        for (int e = threadIdx.x; e < (hi - lo) * a.batch; e += NW * 32) {
-          const int lrow = lo + e / a.batch, col = e % a.batch;
+      for (int u0 = 0; u0 < (fuse_r ? 1 : my_rbs); ++u0) {       // my_rbs <= 2 when S > 1
+        const int rb = u0 == 0 ? rbs_r[0] : rbs_r[1];
+        for (int e = threadIdx.x; e < (hi - lo) * batch_r; e += NW * 32) {
+          const int lrow = lo + e / batch_r, col = e % batch_r;
           const int row = rb * ROWS + lrow;
           float v = 0.f;
-          for (int p = 0; p < nrank; ++p) v += xchg[((u0 * a.S + p) * per + lrow - lo) * 8 + col];
-          if (a.fuse) {                                            // v is the gate; the up partials follow
+          for (int p = 0; p < nrank; ++p) v += xchg[((u0 * S_r + p) * per + lrow - lo) * 8 + col];
+          if (fuse_r) {                                            // v is the gate; the up partials follow
             float u = 0.f;
-            for (int p = 0; p < nrank; ++p) u += xchg[((a.S + p) * per + lrow - lo) * 8 + col];
+            for (int p = 0; p < nrank; ++p) u += xchg[((S_r + p) * per + lrow - lo) * 8 + col];
             v = silu(v) * u;
           }
-          if (row < P.n)
-            P.y[static_cast<int64_t>(col) * P.n + row] =
+          if (row < n_r)
+            y_r[static_cast<int64_t>(col) * n_r + row] =
                 XBF ? __bfloat16_as_ushort(__float2bfloat16_rn(v)) : __half_as_ushort(__float2half_rn(v));
         }
       }
