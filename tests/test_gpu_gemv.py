@@ -230,3 +230,15 @@ def test_gemv_two_row_blocks_per_cluster(fmt, batch):
     y_ref, a = oracle_products(fmt, codes, scales, k, x.cpu())
     check_products(y, y_ref, a, f"{fmt} {n}x{k} batch={batch}", cols=rows)
 
+
+
+@pytest.mark.parametrize("xdt", ["f16", "bf16"])
+def test_gemv_1bit_table_many_row_blocks(xdt):
+    """1-bit at batch 1 (table form) with 299 row blocks on persistent CTAs, the last one ragged:
+    every row is checked."""
+    n, k = 299 * 128 - 50, 1024
+    pw, codes, scales = _packed("1bit", n, k, seed=71)
+    x = synth.activations(1, k, xdt, seed=72).cuda()
+    y = _run_guarded(pw, x)
+    y_ref, a = oracle_products("1bit", codes, scales, k, x.cpu())
+    check_products(y, y_ref, a, f"1-bit {n}x{k} persistent")

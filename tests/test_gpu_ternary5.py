@@ -138,3 +138,15 @@ def test_gemv_ternary5_batched(batch):
             y_ref, a = orc.matvec(orc.FMT_TERNARY5, refs[i][0], refs[i][1], k, xv)
             check_products(y, y_ref, a, f"ternary5 batched {group} problem {i} batch={batch}")
 
+
+
+def test_gemv_ternary5_many_row_blocks():
+    """Five per byte at batch 1 with 299 row blocks on persistent CTAs, the last one ragged."""
+    n, k = 299 * 128 - 77, 1024
+    t, s = _inputs(n, k, seed=80)
+    pw = tensors.pack_ternary5(t.cuda(), s.cuda())
+    codes, scales = orc.pack_ternary5(t.numpy(), s.numpy().view(np.uint16))
+    x = synth.activations(1, k, "bf16", seed=81).cuda()
+    y = _run_guarded(pw, x)
+    y_ref, a = orc.matvec(orc.FMT_TERNARY5, codes, scales, k, orc.decode_activation_bits(u16(x), "bf16"))
+    check_products(y, y_ref, a, f"ternary5 {n}x{k} persistent")
