@@ -99,6 +99,44 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_t5_kernel(const uint8_t* __r
   for (int r = 0; r < kRowsPerWarp; ++r)
 #pragma unroll
     for (int b = 0; b < BP; ++b) acc[r][b] = 0.f;
+  // bfloat16 x reaches 3.4e38, where FP32 partial sums overflow although the product is finite:
+  // a column whose largest magnitude is 2^100 or more is scaled down by an exact power of two
+  // (largest magnitude below 2^100) and its results scaled back.  One pass over x finds the
+  // columns' largest exponents.
+  __shared__ uint32_t cmax[8];
+  float xsc[BP], ysc[BP];
+#pragma unroll
+  for (int b = 0; b < BP; ++b) xsc[b] = ysc[b] = 1.f;
+  if (XBF) {
+    if (threadIdx.x < 8) cmax[threadIdx.x] = 0u;
+    __syncthreads();
+    uint32_t mx[BP];
+#pragma unroll
+    for (int b = 0; b < BP; ++b) mx[b] = 0u;
+    for (int w8 = threadIdx.x; w8 < k / 8; w8 += blockDim.x)
+#pragma unroll
+      for (int b = 0; b < BP; ++b)
+        if (b < batch) {
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + static_cast<int64_t>(b) * k) + w8);
+          const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) mx[b] = max(mx[b], max((u[i] << 16) & 0x7f800000u, u[i] & 0x7f800000u));
+        }
+#pragma unroll
+    for (int b = 0; b < BP; ++b) {
+      for (int o = 16; o > 0; o >>= 1) mx[b] = max(mx[b], __shfl_xor_sync(0xffffffffu, mx[b], o));
+      if (lane == 0 && b < batch) atomicMax(&cmax[b], mx[b]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int b = 0; b < BP; ++b) {
+      const int e = static_cast<int>(cmax[b] >> 23) - 127;
+      if (e >= 100) {
+        xsc[b] = __uint_as_float(static_cast<uint32_t>(127 + 99 - e) << 23);
+        ysc[b] = __uint_as_float(static_cast<uint32_t>(127 - 99 + e) << 23);
+      }
+    }
+  }
 
   for (int c0 = 0; c0 < k; c0 += kKC) {
     const int kc = min(kKC, k - c0);
@@ -108,8 +146,14 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_t5_kernel(const uint8_t* __r
       float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
       if (b < batch) {
         const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + static_cast<int64_t>(b) * k + c0) + w8);
-        lo = make_float4(act<XBF>(v.x & 0xffffu), act<XBF>(v.x >> 16), act<XBF>(v.y & 0xffffu), act<XBF>(v.y >> 16));
-        hi = make_float4(act<XBF>(v.z & 0xffffu), act<XBF>(v.z >> 16), act<XBF>(v.w & 0xffffu), act<XBF>(v.w >> 16));
+        float f = 1.f;                                         // the column's power-of-two scale
+#pragma unroll
+        for (int bb = 0; bb < BP; ++bb)
+          if (bb == b) f = xsc[bb];
+        lo = make_float4(act<XBF>(v.x & 0xffffu) * f, act<XBF>(v.x >> 16) * f, act<XBF>(v.y & 0xffffu) * f,
+                         act<XBF>(v.y >> 16) * f);
+        hi = make_float4(act<XBF>(v.z & 0xffffu) * f, act<XBF>(v.z >> 16) * f, act<XBF>(v.w & 0xffffu) * f,
+                         act<XBF>(v.w >> 16) * f);
       }
       float4* d = reinterpret_cast<float4*>(xs + b * kKC + 8 * w8);
       d[0] = lo;
@@ -175,6 +219,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_t5_kernel(const uint8_t* __r
       float v = acc[r][b];
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      v *= ysc[b];
       if (lane == 0 && row < n && b < batch)
         y[static_cast<int64_t>(b) * n + row] =
             XBF ? __bfloat16_as_ushort(__float2bfloat16_rn(v)) : __half_as_ushort(__float2half_rn(v));

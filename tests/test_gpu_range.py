@@ -26,18 +26,20 @@ def _packed(fmt, n, k, seed):
         w = synth.weights_fp32(n, k, 0.002, seed)
         return tensors.pack_1bit(w.cuda()), orc.pack_1bit(w.numpy())
     t, s = synth.ternary_codes(n, k, seed), synth.ternary_scales_bits(n, k, 0.02, seed + 1)
+    if fmt == "ternary5":
+        return tensors.pack_ternary5(t.cuda(), s.cuda()), orc.pack_ternary5(t.numpy(), s.numpy().view(np.uint16))
     return tensors.pack_ternary(t.cuda(), s.cuda()), orc.pack_ternary(t.numpy(), s.numpy().view(np.uint16))
 
 
 def _oracle(fmt, codes, scales, k, x):
     xdt = "bf16" if x.dtype == torch.bfloat16 else "f16"
-    f = orc.FMT_1BIT if fmt == "1bit" else orc.FMT_TERNARY
+    f = {"1bit": orc.FMT_1BIT, "ternary": orc.FMT_TERNARY, "ternary5": orc.FMT_TERNARY5}[fmt]
     y_ref, a = orc.matvec(f, codes, scales, k, orc.decode_activation_bits(u16(x.cpu()), xdt))
     assert np.all(np.abs(y_ref) + orc.tolerance(y_ref, a) < FMAX[xdt]), "test input overflows the output format"
     return y_ref, a
 
 
-@pytest.mark.parametrize("fmt", ["1bit", "ternary"])
+@pytest.mark.parametrize("fmt", ["1bit", "ternary", "ternary5"])
 @pytest.mark.parametrize("xdt", ["bf16", "f16"])
 @pytest.mark.parametrize("n,k", [(300, 2176), (1100, 5120)])
 def test_gemv_wide_range(fmt, xdt, n, k):
@@ -58,7 +60,7 @@ def test_gemv_wide_range(fmt, xdt, n, k):
     assert lb.lb_device_error(clear=True) == 0
 
 
-@pytest.mark.parametrize("fmt", ["1bit", "ternary"])
+@pytest.mark.parametrize("fmt", ["1bit", "ternary", "ternary5"])
 @pytest.mark.parametrize("batch", [1, 5])
 def test_gemv_batched_wide_range(fmt, batch):
     shapes = [(300, 2176), (17, 640), (1100, 512)]
