@@ -150,3 +150,25 @@ def test_gemv_ternary5_many_row_blocks():
     y = _run_guarded(pw, x)
     y_ref, a = orc.matvec(orc.FMT_TERNARY5, codes, scales, k, orc.decode_activation_bits(u16(x), "bf16"))
     check_products(y, y_ref, a, f"ternary5 {n}x{k} persistent")
+
+
+def test_gemv_ternary5_c4t_gate_up_grouped():
+    """The 27B-class gate and up matrices (17408 x 5120 each) stored five per byte in one grouped
+    launch on one x at batch 1: persistent CTAs over both matrices' row blocks with one table
+    build per CTA.  Sampled rows of both outputs, including every row block's first and last."""
+    wl = synth.WORKLOADS["c4t"]
+    idx = [next(i for i, m in enumerate(wl.matrices) if m.name == nm) for nm in ("gate", "up")]
+    inps = [synth.matrix_inputs(wl, i) for i in idx]
+    pws = [tensors.pack_ternary5(inp["t"].cuda(), inp["s"].cuda()) for inp in inps]
+    x = synth.workload_activations(wl, idx[0], 1).cuda()
+    ys = tensors.gemv_batched([(pw, x) for pw in pws])
+    torch.cuda.synchronize()
+    n, k = wl.matrices[idx[0]].n, wl.matrices[idx[0]].k
+    rb = np.arange(0, n, 128)
+    rng = np.random.default_rng(17)
+    rows = np.unique(np.concatenate([rb, rb + 127, rng.integers(0, n, 600)]))
+    xv = orc.decode_activation_bits(u16(x), "bf16")
+    for name, inp, y in zip(("gate", "up"), inps, ys):
+        codes, scales = orc.pack_ternary5(inp["t"].numpy()[rows], inp["s"].numpy().view(np.uint16)[rows])
+        y_ref, a = orc.matvec(orc.FMT_TERNARY5, codes, scales, k, xv)
+        check_products(y, y_ref, a, f"c4t {name} ternary5 grouped", cols=rows)
