@@ -1,4 +1,5 @@
-// Decode GEMV / small-batch GEMV against packed 1-bit or ternary weights (batch 1..8).
+// Decode GEMV / small-batch GEMV against packed 1-bit or ternary weights (batch 1..8; ternary in
+// 2-bit fields, or five per byte at batch 1).
 //
 //   y[b][n] = sum_g s[n][g] * sum_{i<128} t[n][128g+i] * x[b][128g+i]
 //
@@ -30,13 +31,20 @@
 //     activation types share the binary16 decode; every element within 2^32 of the column maximum
 //     is converted exactly.
 //
+// Lookup-table form (batch 1, BP = 0): thread = weight row, and the activations become tables of
+// signed sums in shared memory, built once per CTA for its K range.  1-bit: per chunk of four
+// activations the 16 sums of +-x, so a code nibble costs one lookup and one FADD.  Five per byte:
+// per byte slot of a group, the 9 sums over its first two weights and the 27 over its last three,
+// so a code byte b costs two lookups (b mod 9, b / 9) and two FADDs.
+//
 // Memory pipeline: a producer warp streams the codes (and scales) of 128-row x 8-group tiles with
 // 2-D TMA loads (128-byte swizzled, so the consumers' fragment reads hit 32 distinct banks) into a
 // ring of shared-memory stages.  Sixteen consumer warps work on the eight 16-row tiles of a row
 // block, two per tile, each taking half of a stage's groups; their partial sums meet in shared
 // memory at the end of the row block.  CTAs are persistent over row blocks.  When a matrix has
-// too few row blocks to fill the GPU, K is split across the CTAs of a thread-block cluster whose
-// partial sums meet in distributed shared memory.  The kernel is launched with programmatic
+// too few row blocks to fill the GPU, K is split across the CTAs of a thread-block cluster: each
+// rank stores its partial sums into the row owner's shared memory with st.async, counted in bytes
+// on the owner's exchange mbarrier, and each owner sums its rows.  The kernel is launched with programmatic
 // dependent launch: weight loads start before griddepcontrol.wait, which guards every read of x
 // and write of y.
 //
