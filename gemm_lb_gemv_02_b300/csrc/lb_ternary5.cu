@@ -8,8 +8,8 @@
 // [N][K/128].  1.625 + 0.125 = 1.75 bits per weight against 2.125 for the 2-bit fields.
 //
 // GEMV  y[b][n] = sum_g s[n][g] * sum_i t[n][128g+i] * x[b][128g+i]  (FP32 accumulation), for
-// batches 2..8 and K not a multiple of 1024 (batch 1 with such K runs the GEMV kernel's
-// lookup-table form instead): a CUDA-core kernel.  A 243-entry shared-memory table turns a code byte into its five digits, one
+// batches 2..8, and at batch 1 when K is not a multiple of 1024 or too long for the tables
+// (otherwise batch 1 runs the GEMV kernel's lookup-table form): a CUDA-core kernel.  A 243-entry shared-memory table turns a code byte into its five digits, one
 // per byte of a 64-bit entry; one byte permute then drops digit f into the low byte of the float
 // 1.5 * 2^23 (whose low mantissa bits are zero), so that float minus (1.5 * 2^23 + 1) is t = f - 1
 // exactly: a digit costs a PRMT and an FADD before its FFMA.  Lane l of a warp
