@@ -468,10 +468,11 @@ def measure_read_probe_rows(lbt, peaks, sel=None):
     return rows
 
 
-SWIGLU_ROWS = (  # row name, workload, batch
+SWIGLU_ROWS = (  # row name, workload, batch[, storage]
     ("swiglu_c2_b1", "c2", 1),
     ("swiglu_c4t_b1", "c4t", 1),
     ("swiglu_c4t_b5", "c4t", 5),
+    ("swiglu_c4t_b1_ternary5", "c4t", 1, "ternary5"),
 )
 
 
@@ -479,7 +480,7 @@ def measure_swiglu_rows(lbt, peaks, sel=None):
     """The feed-forward gate / up pair: h = silu(W_gate x) * (W_up x) in one fused launch, against
     the same pair issued as one grouped launch of two GEMVs (g and u written out)."""
     rows = {}
-    for name, key, b in SWIGLU_ROWS:
+    for name, key, b, *storage in SWIGLU_ROWS:
         if not _want(name, sel):
             continue
         wl = synth.WORKLOADS[key]
@@ -487,8 +488,12 @@ def measure_swiglu_rows(lbt, peaks, sel=None):
         base = []
         for i in idx:
             inp = synth.matrix_inputs(wl, i)
-            base.append(lbt.pack_1bit(inp["w"].cuda()) if wl.fmt == "1bit"
-                        else lbt.pack_ternary(inp["t"].cuda(), inp["s"].cuda()))
+            if wl.fmt == "1bit":
+                base.append(lbt.pack_1bit(inp["w"].cuda()))
+            elif storage and storage[0] == "ternary5":
+                base.append(lbt.pack_ternary5(inp["t"].cuda(), inp["s"].cuda()))
+            else:
+                base.append(lbt.pack_ternary(inp["t"].cuda(), inp["s"].cuda()))
         per_copy = _gemv_bytes(base[0], b) + _gemv_bytes(base[1], b)
         copies = _copies_for(per_copy)
         pairs = [base] + [[_clone(pw) for pw in base] for _ in range(copies - 1)]
@@ -515,7 +520,8 @@ def measure_swiglu_rows(lbt, peaks, sel=None):
         ms_c = _time_graph(g_c, reps=3) / steps
         by = per_copy - 2 * b * base[0].k - 2 * b * n     # x read once, one output vector
         gbs = by / (ms_f * 1e-3) / 1e9
-        rows[name] = {"shape": [n, base[0].k], "fmt": wl.fmt, "batch": b, "us_per_pair": round(ms_f * 1e3, 2),
+        rows[name] = {"shape": [n, base[0].k], "fmt": storage[0] if storage else wl.fmt, "batch": b,
+                      "us_per_pair": round(ms_f * 1e3, 2),
                       "GB_s": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 3),
                       "unfused_grouped_us": round(ms_u * 1e3, 2),
                       "unfused_grouped_plus_combine_us": round(ms_c * 1e3, 2),

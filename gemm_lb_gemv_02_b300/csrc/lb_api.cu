@@ -250,14 +250,15 @@ lb_status lb_gemv_swiglu(const lb_weight* Wg, const lb_weight* Wu, const void* x
   s = check_weight(Wu);
   if (s != LB_OK) return s;
   if (Wg->fmt != Wu->fmt) return fail(LB_ERR_UNSUPPORTED, "gate and up must have the same format");
-  if (Wg->fmt == LB_FMT_TERNARY5_G128)
-    return fail(LB_ERR_UNSUPPORTED, "lb_gemv_swiglu takes the 1-bit and 2-bit ternary formats");
   if (Wg->n != Wu->n || Wg->k != Wu->k)
     return fail(LB_ERR_SHAPE, "gate (%lld x %lld) and up (%lld x %lld) must have the same shape", (long long)Wg->n,
                 (long long)Wg->k, (long long)Wu->n, (long long)Wu->k);
   if (!x || !h) return fail(LB_ERR_NULL, "x and h must be non-NULL");
   if (!valid_dtype(xdt)) return fail(LB_ERR_DTYPE, "unknown activation dtype %d", xdt);
   if (batch < 1 || batch > 8) return fail(LB_ERR_SHAPE, "batch must be in [1, 8] (got %d)", batch);
+  if (Wg->fmt == LB_FMT_TERNARY5_G128 && !lb::gemv_t5_lut_ok(*Wg, batch))
+    return fail(LB_ERR_UNSUPPORTED,
+                "lb_gemv_swiglu on five-per-byte weights runs at batch 1 with k a multiple of 1024 (k <= 40960)");
   if (!lb::aligned16(x) || !lb::aligned16(h)) return fail(LB_ERR_ALIGN, "x and h must be 16-byte aligned");
   return lb::launch_gemv_swiglu(*Wg, *Wu, x, xdt, batch, h, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -1337,6 +1337,8 @@ lb_status launch_gemv_swiglu(const lb_weight& Wg, const lb_weight& Wu, const voi
   const uint16_t* xs = static_cast<const uint16_t*>(x);
   uint16_t* hs = static_cast<uint16_t*>(h);
   const bool bf = xdt == LB_BF16;
+  if (Wg.fmt == LB_FMT_TERNARY5_G128)                              // callers checked gemv_t5_lut_ok
+    return bf ? launch_pair<3, true, 0>(Wg, Wu, xs, batch, hs, st) : launch_pair<3, false, 0>(Wg, Wu, xs, batch, hs, st);
   if (Wg.fmt == LB_FMT_1BIT_G128)
     return bf ? launch_pb<1, true>(Wg, Wu, xs, batch, hs, st) : launch_pb<1, false>(Wg, Wu, xs, batch, hs, st);
   return bf ? launch_pb<2, true>(Wg, Wu, xs, batch, hs, st) : launch_pb<2, false>(Wg, Wu, xs, batch, hs, st);

@@ -206,7 +206,8 @@ lb_status lb_gemv_batched(const lb_gemv_problem* problems, int count, int xdt, i
  * (or cluster) per 128-row block runs the block's gate rows and then its up rows on one prologue of
  * x, so the pair costs one launch and one x prologue.
  *
- * Wg, Wu   : packed matrices of the same format and shape (N x K).
+ * Wg, Wu   : packed matrices of the same format and shape (N x K).  Five per byte: batch 1 with K a
+ *            multiple of 1024 (K <= 40960; the lookup-table form), LB_ERR_UNSUPPORTED otherwise.
  * x        : device [batch][K] of `xdt`, 16-byte aligned;  h : device [batch][N] of `xdt`, 16-byte
  *            aligned, caller-owned, not overlapping x.
  * batch    : 1 .. 8, with the K limits of lb_gemv;  N <= 65535 * 128.

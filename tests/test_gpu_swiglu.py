@@ -23,6 +23,8 @@ def _inputs(fmt, n, k, seed):
 def _device(fmt, inp):
     if fmt == "1bit":
         return tensors.pack_1bit(inp["w"].cuda())
+    if fmt == "ternary5":
+        return tensors.pack_ternary5(inp["t"].cuda(), inp["s"].cuda())
     return tensors.pack_ternary(inp["t"].cuda(), inp["s"].cuda())
 
 
@@ -30,6 +32,8 @@ def _oracle(fmt, inp, rows=None):
     sel = slice(None) if rows is None else rows
     if fmt == "1bit":
         return orc.pack_1bit(inp["w"].numpy()[sel])
+    if fmt == "ternary5":
+        return orc.pack_ternary5(inp["t"].numpy()[sel], inp["s"].numpy().view(np.uint16)[sel])
     return orc.pack_ternary(inp["t"].numpy()[sel], inp["s"].numpy().view(np.uint16)[sel])
 
 
@@ -38,7 +42,7 @@ def _check(fmt, ig, iu, h, x, rows=None):
     cg, sg = _oracle(fmt, ig, rows)
     cu, su = _oracle(fmt, iu, rows)
     xv = orc.decode_activation_bits(u16(x), xdt)
-    f = orc.FMT_1BIT if fmt == "1bit" else orc.FMT_TERNARY
+    f = {"1bit": orc.FMT_1BIT, "ternary": orc.FMT_TERNARY, "ternary5": orc.FMT_TERNARY5}[fmt]
     h_ref, g, a_g, u, a_u = orc.swiglu(f, cg, sg, cu, su, ig["w"].shape[1] if fmt == "1bit" else ig["t"].shape[1], xv)
     hv = orc.decode_activation_bits(u16(h), xdt)
     if rows is not None:
@@ -109,3 +113,38 @@ def test_swiglu_c4t_block_sampled():
         torch.cuda.synchronize()
         assert lb.lb_device_error(clear=True) == 0
         _check("ternary", ig, iu, h, x, rows=rows)
+
+
+@pytest.mark.parametrize("xdt", ["f16", "bf16"])
+@pytest.mark.parametrize("n,k", [(100, 1024), (333, 4096), (64, 16384), (6144, 2048)])
+def test_swiglu_ternary5(xdt, n, k):
+    """Five-per-byte gate / up at batch 1 (the lookup-table form with one table build for both
+    units; 16384-wide K splits over a cluster).  Other batches and K not a multiple of 1024 are
+    refused."""
+    ig, iu = _inputs("ternary5", n, k, seed=n + k), _inputs("ternary5", n, k, seed=n + k + 7)
+    pg, pu = _device("ternary5", ig), _device("ternary5", iu)
+    x = synth.activations(1, k, xdt, seed=n + 1).cuda()
+    h = _run_guarded(pg, pu, x)
+    _check("ternary5", ig, iu, h, x)
+    with pytest.raises(lb.LBError) as e:
+        tensors.gemv_swiglu(pg, pu, synth.activations(2, k, xdt, seed=1).cuda())
+    assert e.value.name == "LB_ERR_UNSUPPORTED"
+
+
+def test_swiglu_ternary5_c4t_sampled():
+    """The 27B-class gate / up pair stored five per byte at batch 1, sampled rows."""
+    wl = synth.WORKLOADS["c4t"]
+    gi = next(i for i, m in enumerate(wl.matrices) if m.name == "gate")
+    ui = next(i for i, m in enumerate(wl.matrices) if m.name == "up")
+    ig, iu = synth.matrix_inputs(wl, gi), synth.matrix_inputs(wl, ui)
+    pg, pu = _device("ternary5", ig), _device("ternary5", iu)
+    n = wl.matrices[gi].n
+    rb = np.arange(0, n, 128)
+    rng = np.random.default_rng(9)
+    rows = np.unique(np.concatenate([rb, rb + 127, rng.integers(0, n, 600)]))
+    x = synth.workload_activations(wl, gi, 1).cuda()
+    h = tensors.gemv_swiglu(pg, pu, x)
+    torch.cuda.synchronize()
+    assert lb.lb_device_error(clear=True) == 0
+    _check("ternary5", ig, iu, h, x, rows=rows)
+
