@@ -142,6 +142,7 @@ __device__ __forceinline__ void trace_ev(int e) {
 #endif
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(NW * 32) : "memory"); }
+constexpr int kBarInit = 10;              // named barrier: the producer's barrier setup -> consumers
 // the two consumer warps of 16-row tile t (named barriers 2 .. NT + 1)
 __device__ __forceinline__ void tile_sync(int t) { asm volatile("bar.sync %0, 64;" ::"r"(2 + t) : "memory"); }
 
@@ -253,20 +254,31 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   const int total_st = my_rbs * nst;
   bool ok = true;
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < L::stages; ++s) {
-      lbdev::mbar_init(&full[s], P.scales_tma ? 1 : 32);         // 32: the lanes store the scales
-      lbdev::mbar_init(&empty[s], NW);
+  // Start-up without a block-wide barrier: the producer warp initialises the pipeline and exchange
+  // barriers itself and starts copying at once, then publishes the barriers on named barrier
+  // kBarInit, on which the consumers wait only before their first stage (they spend the time on
+  // x); the consumers zero the column maxima among themselves.  (With a block barrier first, a
+  // traced small launch issued its first copy ~2.9 kcyc after the start and its consumers then
+  // waited ~1.4 kcyc for it.)  K split: every thread also arrives on the cluster barrier after
+  // this, and the consumers wait on it before their first remote store, so that no CTA's exchange
+  // barrier is used before it is initialised (by then it has long completed).
+  if (warp == NW) {
+    if (lane == 0) {
+      for (int s = 0; s < L::stages; ++s) {
+        lbdev::mbar_init(&full[s], P.scales_tma ? 1 : 32);       // 32: the lanes store the scales
+        lbdev::mbar_init(&empty[s], NW);
+      }
+      lbdev::mbar_init(xbar, 1);
+      lbdev::fence_mbar_init();
     }
-    lbdev::mbar_init(xbar, 1);
-    lbdev::fence_mbar_init();
+    __syncwarp();
+    asm volatile("bar.arrive %0, %1;" ::"n"(kBarInit), "n"((NW + 1) * 32) : "memory");
+    if (a.S > 1) cluster_arrive();
+  } else {
+    if (threadIdx.x < 8) reinterpret_cast<uint32_t*>(sm + L::colf)[8 + threadIdx.x] = 0u;   // column maxima
+    consumer_sync();
+    if (a.S > 1) cluster_arrive();
   }
-  if (threadIdx.x < 8) reinterpret_cast<uint32_t*>(sm + L::colf)[8 + threadIdx.x] = 0u;   // column maxima
-  __syncthreads();
-  // K split: every thread arrives on the cluster barrier now and the consumers wait on it before
-  // their first remote store, so that no CTA's exchange barrier is used before it is initialised
-  // (by then the barrier has long completed, so the wait costs nothing)
-  if (a.S > 1) cluster_arrive();
 
   if (warp == NW) {
     // ======================= producer: weights do not depend on earlier kernels, so no wait.
@@ -437,6 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     }
     consumer_sync();
     LB_TRACE(threadIdx.x == 0, 4);
+    asm volatile("bar.sync %0, %1;" ::"n"(kBarInit), "n"((NW + 1) * 32) : "memory");   // the producer's barriers
     if (a.S > 1) cluster_wait();                                   // every exchange barrier is initialised
 
     const int rq = warp & 3, kq = warp >> 2;                      // rows 32 rq .., groups 2 kq, 2 kq + 1
@@ -691,6 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
       reinterpret_cast<uint4*>(xs)[i] = make_uint4(0u, 0u, 0u, 0u);  // x of the padding groups: zero
     consumer_sync();
     LB_TRACE(threadIdx.x == 0, 4);
+    asm volatile("bar.sync %0, %1;" ::"n"(kBarInit), "n"((NW + 1) * 32) : "memory");   // the producer's barriers
     if (a.S > 1) cluster_wait();                                   // every exchange barrier is initialised
 
     uint32_t tok;                                      // orders the private-region loads after the barrier
