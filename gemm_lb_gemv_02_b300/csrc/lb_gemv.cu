@@ -256,12 +256,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 
   // Start-up without a block-wide barrier: the producer warp initialises the pipeline and exchange
   // barriers itself and starts copying at once, then publishes the barriers on named barrier
-  // kBarInit, on which the consumers wait only before their first stage (they spend the time on
-  // x); the consumers zero the column maxima among themselves.  (With a block barrier first, a
-  // traced small launch issued its first copy ~2.9 kcyc after the start and its consumers then
-  // waited ~1.4 kcyc for it.)  K split: every thread also arrives on the cluster barrier after
-  // this, and the consumers wait on it before their first remote store, so that no CTA's exchange
-  // barrier is used before it is initialised (by then it has long completed).
+  // kBarInit; the consumers zero the column maxima among themselves and wait on kBarInit just
+  // before griddepcontrol.wait, so that inside a launch chain the wait is hidden behind the
+  // previous kernel.  (With a block barrier first, a traced small launch issued its first copy
+  // ~2.9 kcyc after the start and its consumers then waited ~1.4 kcyc for it.)  K split: every
+  // thread also arrives on the cluster barrier after this, and the consumers wait on it before
+  // their first stage, so that no CTA's exchange barrier is used before it is initialised (by then
+  // it has long completed).
   if (warp == NW) {
     if (lane == 0) {
       for (int s = 0; s < L::stages; ++s) {
@@ -345,6 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     // [2^15, 2^16)) and the result scaled back.
     float* colf = reinterpret_cast<float*>(sm + L::colf);
     float* tab = reinterpret_cast<float*>(sm + L::xs(gpc));
+    asm volatile("bar.sync %0, %1;" ::"n"(kBarInit), "n"((NW + 1) * 32) : "memory");   // the producer's barriers
     griddep_wait();                                   // x is read and y written only after this
     LB_TRACE(threadIdx.x == 0, 3);
     const int chunks = ng > 0 ? ng * 32 : 0;
@@ -449,7 +451,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     }
     consumer_sync();
     LB_TRACE(threadIdx.x == 0, 4);
-    asm volatile("bar.sync %0, %1;" ::"n"(kBarInit), "n"((NW + 1) * 32) : "memory");   // the producer's barriers
     if (a.S > 1) cluster_wait();                                   // every exchange barrier is initialised
 
     const int rq = warp & 3, kq = warp >> 2;                      // rows 32 rq .., groups 2 kq, 2 kq + 1
@@ -579,6 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     float* colf = reinterpret_cast<float*>(sm + L::colf);            // [8] factors, then [8] maxima
     float* cneg = reinterpret_cast<float*>(sm + L::cneg);            // [gpc][4][4]
     uint8_t* xs = sm + L::xs(gpc);
+    asm volatile("bar.sync %0, %1;" ::"n"(kBarInit), "n"((NW + 1) * 32) : "memory");   // the producer's barriers
     griddep_wait();                                   // x is read and y written only after this
     LB_TRACE(threadIdx.x == 0, 3);
 
@@ -704,7 +706,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
       reinterpret_cast<uint4*>(xs)[i] = make_uint4(0u, 0u, 0u, 0u);  // x of the padding groups: zero
     consumer_sync();
     LB_TRACE(threadIdx.x == 0, 4);
-    asm volatile("bar.sync %0, %1;" ::"n"(kBarInit), "n"((NW + 1) * 32) : "memory");   // the producer's barriers
     if (a.S > 1) cluster_wait();                                   // every exchange barrier is initialised
 
     uint32_t tok;                                      // orders the private-region loads after the barrier
