@@ -104,6 +104,11 @@ __device__ __forceinline__ uint32_t cluster_rank() {
   return r;
 }
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+// An arrival that releases nothing: for a thread whose only writes the cluster must see are
+// mbarrier initialisations, which fence.mbarrier_init.release.cluster has already released.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 // v into the shared memory of cluster CTA `rank`, at the image of `local_addr` there; the store
 // counts its 4 bytes on that CTA's mbarrier at the image of `local_bar` (complete_tx), which makes
@@ -120,9 +125,11 @@ __device__ __forceinline__ void st_async_f32(uint32_t local_addr, uint32_t local
 // {%globaltimer, clock64} of the moment one fixed thread passed a point of the kernel.  Events:
 // 0 CTA start, 1 producer's first copy issued, 2 producer's last copy issued, 3 consumers past
 // griddepcontrol.wait, 4 x prologue done, 5 + i (i < 16) warp 0 got stage i, 21 + j (j < 8) warp
-// 0 finished unit j, 29 consumers done, 30 CTA end; slot 31 holds {gridDim.x, gridDim.y}.
+// 0 finished unit j, 29 consumers done, 30 CTA end; producer start-up: 31 barriers initialised
+// and fenced, 32 past its start-up arrivals, 33 at the start of its copy loop, 34 first slot granted;
+// the last slot holds {gridDim.x, gridDim.y}.
 #ifdef LB_GEMV_TRACE
-constexpr int kTraceCtas = 2048, kTraceEvents = 32;
+constexpr int kTraceCtas = 2048, kTraceEvents = 40;
 __device__ unsigned long long g_gemv_trace[kTraceCtas][kTraceEvents][2];
 __device__ __forceinline__ void trace_ev(int e) {
   const unsigned cta = blockIdx.y * gridDim.x + blockIdx.x;
@@ -262,8 +269,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
   // ~2.9 kcyc after the start and its consumers then waited ~1.4 kcyc for it.)  K split: every
   // thread also arrives on the cluster barrier after this, and the consumers wait on it before
   // their first stage, so that no CTA's exchange barrier is used before it is initialised (by then
-  // it has long completed).
+  // it has long completed).  The producer's tensor-map prefetches come first, so that the
+  // descriptor fetches overlap the barrier set-up, and its cluster arrival is relaxed (the init
+  // fence already released the barriers; a releasing arrival held the producer ~0.7-1.0 kcyc
+  // before its first copy in traced 3-CTA-cluster launches).
   if (warp == NW) {
+    if (lane == 0)
+      for (int i = 0; i < a.count; ++i)
+        if (i == pi || a.fuse || a.shared) {
+          lbdev::prefetch_tmap(&a.p[i].tm_codes);
+          if (P.scales_tma) lbdev::prefetch_tmap(&a.p[i].tm_scales);
+        }
     if (lane == 0) {
       for (int s = 0; s < L::stages; ++s) {
         lbdev::mbar_init(&full[s], P.scales_tma ? 1 : 32);       // 32: the lanes store the scales
@@ -271,10 +287,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
       }
       lbdev::mbar_init(xbar, 1);
       lbdev::fence_mbar_init();
+      LB_TRACE(true, 31);
     }
     __syncwarp();
     asm volatile("bar.arrive %0, %1;" ::"n"(kBarInit), "n"((NW + 1) * 32) : "memory");
-    if (a.S > 1) cluster_arrive();
+    if (a.S > 1) cluster_arrive_relaxed();
+    LB_TRACE(lane == 0, 32);
   } else {
     if (threadIdx.x < 8) reinterpret_cast<uint32_t*>(sm + L::colf)[8 + threadIdx.x] = 0u;   // column maxima
     consumer_sync();
@@ -287,12 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     // 32 lanes load the stage's scales from global memory, store them in the slot in the TMA
     // box's layout and arrive on the stage's barrier themselves.
     const bool stma = P.scales_tma != 0;
-    if (lane == 0)
-      for (int i = 0; i < a.count; ++i)
-        if (i == pi || a.fuse || a.shared) {
-          lbdev::prefetch_tmap(&a.p[i].tm_codes);
-          if (stma) lbdev::prefetch_tmap(&a.p[i].tm_scales);
-        }
+    LB_TRACE(lane == 0, 33);
     const uint32_t bytes = static_cast<uint32_t>(FT::nb * FT::box + (stma ? kScaleBox : 0));
     if (stma ? lane == 0 : true) {
       for (int st = 0; st < total_st && !a.test_fault; ++st) {
@@ -301,6 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
           ok = false;
           break;
         }
+        LB_TRACE(lane == 0 && st == 0, 34);
         const int row0 = unit_rb(st / nst) * ROWS;
         const Prob& PU = a.p[unit_prob(st / nst)];                 // the matrix of this unit
         const int g0 = g_begin + (st % nst) * GS;

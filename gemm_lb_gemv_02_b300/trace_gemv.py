@@ -33,8 +33,9 @@ LAYERS = {
     "c4t": [["q"], ["o"], ["gate", "up"], ["down"]],
     "c4b": [["q"], ["o"], ["gate", "up"], ["down"]],
 }
-CTAS, EVENTS = 2048, 32
+CTAS, EVENTS = 2048, 40
 EV_START, EV_COPY0, EV_COPYN, EV_GRIDDEP, EV_PROLOGUE, EV_STAGE0, EV_UNIT0, EV_DONE, EV_END = 0, 1, 2, 3, 4, 5, 21, 29, 30
+EV_P_INIT, EV_P_ARRIVED, EV_P_LOOP, EV_P_SLOT0 = 31, 32, 33, 34
 
 
 def _pct(v, q):
@@ -69,6 +70,11 @@ def summarize(tr: np.ndarray, clock_ghz: float) -> str:
     kc = lambda a, b: np.where((cyc[:, a] > 0) & (cyc[:, b] > 0), (cyc[:, b] - cyc[:, a]) / 1e3, np.nan)
     row("CTA start after the first CTA's start", (ns[:, EV_START] - t0) / 1e3, "us")
     row("start -> producer's first copy issued", kc(EV_START, EV_COPY0), "kcyc")
+    row("  producer: start -> barriers initialised and fenced", kc(EV_START, EV_P_INIT), "kcyc")
+    row("  producer: -> past its start-up arrivals", kc(EV_P_INIT, EV_P_ARRIVED), "kcyc")
+    row("  producer: -> at the start of its copy loop", kc(EV_P_ARRIVED, EV_P_LOOP), "kcyc")
+    row("  producer: -> first slot granted", kc(EV_P_LOOP, EV_P_SLOT0), "kcyc")
+    row("  producer: -> first copy issued", kc(EV_P_SLOT0, EV_COPY0), "kcyc")
     row("start -> consumers past griddepcontrol.wait", us(EV_START, EV_GRIDDEP), "us")
     row("griddepcontrol.wait -> x prologue done", kc(EV_GRIDDEP, EV_PROLOGUE), "kcyc")
     row("x prologue done -> first stage's data ready", kc(EV_PROLOGUE, EV_STAGE0), "kcyc")
