@@ -55,6 +55,10 @@ def summarize(tr: np.ndarray, clock_ghz: float) -> str:
     if len(live) == 0:
         return "no CTA recorded a start and an end\n"
     ns, cyc = ns[live], cyc[live]
+    # events an earlier launch of the chain left in slots this launch does not reach (fewer stages
+    # or units) predate the CTA's start: drop them
+    stale = ns < ns[:, EV_START:EV_START + 1]
+    ns, cyc = np.where(stale, 0, ns), np.where(stale, 0, cyc)
     t0 = ns[:, EV_START].min()
     span = (ns[:, EV_END].max() - t0) / 1e3
     lines = [f"grid {int(grid[0, 0])} x {int(grid[0, 1])}; CTAs traced: {len(live)}; "
