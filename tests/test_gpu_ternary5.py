@@ -54,7 +54,7 @@ def test_gemv_ternary5_shapes(xdt, n, k):
     t, s = _inputs(n, k, seed=2 * n + k)
     pw = tensors.pack_ternary5(t.cuda(), s.cuda())
     codes, scales = orc.pack_ternary5(t.numpy(), s.numpy().view(np.uint16))
-    for batch in (1, 2, 3, 5, 8):
+    for batch in (1, 2, 3, 4, 5, 6, 7, 8):
         x = synth.activations(batch, k, xdt, seed=n + batch).cuda()
         y = _run_guarded(pw, x)
         xv = orc.decode_activation_bits(u16(x), xdt)
